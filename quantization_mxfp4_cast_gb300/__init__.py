@@ -1,0 +1,229 @@
+"""Thin ctypes binding of libmxfp4.so, the GB300 (sm_103a) MXFP4 training-GEMM
+library whose C ABI is declared in include/mxfp4.h.
+
+The functions carry the C entry points' names and only marshal arguments:
+torch tensors give device pointers, the current torch stream is passed as the
+launch stream, and outputs not supplied by the caller are allocated with
+torch.empty.  All arithmetic runs in the library's CUDA kernels; there is no
+CPU or PyTorch fallback.  If the library has not been built, every call raises.
+
+Operations (jax-aiter README, "Supported ops" table): MXFP4 Cast (row-wise and
+dual), FP4 GEMM low-level (pre-quantized operands), FP4 GEMM training
+(forward, dA, dB with BF16 in/out).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG_DIR, "libmxfp4.so")
+
+MXFP4_OK = 0
+MXFP4_HADAMARD_ROW = 1
+MXFP4_HADAMARD_COL = 2
+MXFP4_SCALE_LINEAR = 4
+MXFP4_OP_FWD, MXFP4_OP_DGRAD, MXFP4_OP_WGRAD = 0, 1, 2
+
+# Every extern "C" symbol declared in include/mxfp4.h.
+ABI_SYMBOLS = (
+    "mxfp4_abi_version", "mxfp4_status_string", "mxfp4_codes_bytes", "mxfp4_scales_bytes",
+    "mxfp4_cast", "mxfp4_cast_dual", "gemm_fp4", "mxfp4_workspace_bytes",
+    "gemm_fp4_bf16_fwd", "gemm_fp4_bf16_dgrad", "gemm_fp4_bf16_wgrad", "mxfp4_device_status",
+)
+
+_lib = None
+_lock = threading.Lock()
+
+
+class Mxfp4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with quantization_mxfp4_cast_gb300.build.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I64, U32, SZ, I = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint32, ctypes.c_size_t,
+                                  ctypes.c_int)
+            sig = {
+                "mxfp4_abi_version": (I, []),
+                "mxfp4_status_string": (ctypes.c_char_p, [I]),
+                "mxfp4_codes_bytes": (SZ, [I64, I64]),
+                "mxfp4_scales_bytes": (SZ, [I64, I64, U32]),
+                "mxfp4_cast": (I, [P, I64, I64, I64, P, P, U32, P]),
+                "mxfp4_cast_dual": (I, [P, I64, I64, I64, P, P, P, P, U32, P]),
+                "gemm_fp4": (I, [P, P, P, P, P, I64, I64, I64, I64, P]),
+                "mxfp4_workspace_bytes": (SZ, [I, I64, I64, I64]),
+                "gemm_fp4_bf16_fwd": (I, [P, P, P, I64, I64, I64, P, SZ, P]),
+                "gemm_fp4_bf16_dgrad": (I, [P, P, P, I64, I64, I64, P, SZ, P]),
+                "gemm_fp4_bf16_wgrad": (I, [P, P, P, I64, I64, I64, U32, P, SZ, P]),
+                "mxfp4_device_status": (I, [I, ctypes.POINTER(I)]),
+            }
+            for name, (res, args) in sig.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().mxfp4_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != MXFP4_OK:
+        raise Mxfp4Error(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors must live on a CUDA device")
+
+
+def _bf16_2d(t, name):
+    if t.dtype != torch.bfloat16 or t.dim() != 2:
+        raise ValueError(f"{name} must be a 2-D bf16 tensor")
+    if t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit column stride")
+
+
+# ----------------------------------------------------------------------------- sizes
+def codes_bytes(rows: int, cols: int) -> int:
+    return lib().mxfp4_codes_bytes(rows, cols)
+
+
+def scales_bytes(rows: int, cols: int, linear: bool = False) -> int:
+    return lib().mxfp4_scales_bytes(rows, cols, MXFP4_SCALE_LINEAR if linear else 0)
+
+
+def workspace_bytes(op: int, M: int, N: int, K: int) -> int:
+    return lib().mxfp4_workspace_bytes(op, M, N, K)
+
+
+# ----------------------------------------------------------------------------- cast
+def mxfp4_cast(x, hadamard: bool = False, linear_scales: bool = False, q=None, sf=None, stream=None):
+    """Row-wise cast of bf16 x[R, C] -> (codes uint8 [R, C/2], scales uint8)."""
+    _bf16_2d(x, "x")
+    _need_cuda(x)
+    R, C = x.shape
+    if q is None:
+        q = torch.empty(R, C // 2, dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.empty(scales_bytes(R, C, linear_scales), dtype=torch.uint8, device=x.device)
+    flags = (MXFP4_HADAMARD_ROW if hadamard else 0) | (MXFP4_SCALE_LINEAR if linear_scales else 0)
+    _check(lib().mxfp4_cast(_ptr(x), R, C, x.stride(0), _ptr(q), _ptr(sf), flags, _stream(stream)),
+           "mxfp4_cast")
+    return q, sf
+
+
+def mxfp4_cast_dual(x, hadamard_row: bool = False, hadamard_col: bool = False,
+                    linear_scales: bool = False, out=None, stream=None):
+    """Row-wise and column-wise (transposed) cast in one pass ->
+    (q_row [R, C/2], sf_row, q_col [C, R/2], sf_col)."""
+    _bf16_2d(x, "x")
+    _need_cuda(x)
+    R, C = x.shape
+    if out is None:
+        dev = x.device
+        out = (torch.empty(R, C // 2, dtype=torch.uint8, device=dev),
+               torch.empty(scales_bytes(R, C, linear_scales), dtype=torch.uint8, device=dev),
+               torch.empty(C, R // 2, dtype=torch.uint8, device=dev),
+               torch.empty(scales_bytes(C, R, linear_scales), dtype=torch.uint8, device=dev))
+    q_row, sf_row, q_col, sf_col = out
+    flags = ((MXFP4_HADAMARD_ROW if hadamard_row else 0) | (MXFP4_HADAMARD_COL if hadamard_col else 0)
+             | (MXFP4_SCALE_LINEAR if linear_scales else 0))
+    _check(lib().mxfp4_cast_dual(_ptr(x), R, C, x.stride(0), _ptr(q_row), _ptr(sf_row), _ptr(q_col),
+                                 _ptr(sf_col), flags, _stream(stream)), "mxfp4_cast_dual")
+    return q_row, sf_row, q_col, sf_col
+
+
+# ----------------------------------------------------------------------------- GEMM
+def gemm_fp4(a, a_sf, b, b_sf, M: int, N: int, K: int, c=None, stream=None):
+    """C[M,N] (bf16) = A . B^T for MXFP4 operands (codes [M, K/2] / [N, K/2],
+    tile-layout scales)."""
+    _need_cuda(a, a_sf, b, b_sf)
+    if c is None:
+        c = torch.empty(M, N, dtype=torch.bfloat16, device=a.device)
+    _check(lib().gemm_fp4(_ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), _ptr(c), M, N, K, c.stride(0),
+                          _stream(stream)), "gemm_fp4")
+    return c
+
+
+def _workspace(op, M, N, K, ws, device):
+    need = workspace_bytes(op, M, N, K)
+    if ws is None:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+    return ws, ws.numel() * ws.element_size()
+
+
+def gemm_fp4_bf16_fwd(x, w, y=None, ws=None, stream=None):
+    """Y[M,N] = X[M,K] . W[N,K]^T through MXFP4 (both cast row-wise)."""
+    _bf16_2d(x, "x"), _bf16_2d(w, "w")
+    _need_cuda(x, w)
+    M, K = x.shape
+    N = w.shape[0]
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    ws, nb = _workspace(MXFP4_OP_FWD, M, N, K, ws, x.device)
+    _check(lib().gemm_fp4_bf16_fwd(_ptr(x), _ptr(w), _ptr(y), M, N, K, _ptr(ws), nb, _stream(stream)),
+           "gemm_fp4_bf16_fwd")
+    return y
+
+
+def gemm_fp4_bf16_dgrad(dy, w, dx=None, ws=None, stream=None):
+    """dX[M,K] = dY[M,N] . W[N,K] through MXFP4 (contraction over N)."""
+    _bf16_2d(dy, "dy"), _bf16_2d(w, "w")
+    _need_cuda(dy, w)
+    M, N = dy.shape
+    K = w.shape[1]
+    if dx is None:
+        dx = torch.empty(M, K, dtype=torch.bfloat16, device=dy.device)
+    ws, nb = _workspace(MXFP4_OP_DGRAD, M, N, K, ws, dy.device)
+    _check(lib().gemm_fp4_bf16_dgrad(_ptr(dy), _ptr(w), _ptr(dx), M, N, K, _ptr(ws), nb,
+                                     _stream(stream)), "gemm_fp4_bf16_dgrad")
+    return dx
+
+
+def gemm_fp4_bf16_wgrad(dy, x, hadamard: bool = True, dw=None, ws=None, stream=None):
+    """dW[N,K] = dY[M,N]^T . X[M,K] through MXFP4 (contraction over tokens M);
+    with hadamard=True both operands get the 32-point transform along M."""
+    _bf16_2d(dy, "dy"), _bf16_2d(x, "x")
+    _need_cuda(dy, x)
+    M, N = dy.shape
+    K = x.shape[1]
+    if dw is None:
+        dw = torch.empty(N, K, dtype=torch.bfloat16, device=dy.device)
+    ws, nb = _workspace(MXFP4_OP_WGRAD, M, N, K, ws, dy.device)
+    flags = MXFP4_HADAMARD_COL if hadamard else 0
+    _check(lib().gemm_fp4_bf16_wgrad(_ptr(dy), _ptr(x), _ptr(dw), M, N, K, flags, _ptr(ws), nb,
+                                     _stream(stream)), "gemm_fp4_bf16_wgrad")
+    return dw
+
+
+def device_status(reset: bool = True) -> int:
+    """The library's device status word (0 = OK, 6 = a GEMM wait timed out)."""
+    v = ctypes.c_int(0)
+    _check(lib().mxfp4_device_status(1 if reset else 0, ctypes.byref(v)), "mxfp4_device_status")
+    return v.value

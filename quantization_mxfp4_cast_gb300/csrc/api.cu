@@ -1,0 +1,260 @@
+// C ABI of the MXFP4 library (declared in include/mxfp4.h): argument
+// validation on the host, workspace carving, and launches on the caller's
+// stream.  Nothing here allocates memory or synchronizes (except
+// mxfp4_device_status, which reads the device status word).
+//
+// Operations: jax-aiter README, "Supported ops" table (MXFP4 Cast, FP4 GEMM
+// low-level, FP4 GEMM training) and "MXFP4 training architecture" (forward =
+// activation cast + weight cast + GEMM; backward = gradient cast + dA GEMM,
+// plus the dB GEMM).
+#include <algorithm>
+
+#include "../../include/mxfp4.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+using mxfp4::CastArgs;
+using mxfp4::GemmArgs;
+
+namespace {
+
+constexpr int64_t kMaxDim = int64_t(1) << 31;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mxfp4_status check_device() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MXFP4_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MXFP4_ERR_CUDA;
+  if (major != 10 || minor != 3) return MXFP4_ERR_UNSUPPORTED_DEVICE;
+  return MXFP4_OK;
+}
+
+mxfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+size_t tile_scale_bytes(int64_t rows, int64_t cols) {
+  return static_cast<size_t>(ceil_div(rows, 128) * ceil_div(cols / 32, 4) * 512);
+}
+
+size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+// Common checks of a bf16 input tensor.
+mxfp4_status check_bf16_in(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx) {
+  if (rows < 0 || cols < 0 || rows > kMaxDim || cols > kMaxDim) return MXFP4_ERR_INVALID_ARG;
+  if (cols % 32 != 0) return MXFP4_ERR_INVALID_ARG;
+  if (ldx < cols) return MXFP4_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return MXFP4_OK;
+  if (x == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (!aligned16(x) || (ldx % 8) != 0) return MXFP4_ERR_MISALIGNED;
+  if (ceil_div(rows, 128) > 65535) return MXFP4_ERR_INVALID_ARG;  // grid.y limit
+  return MXFP4_OK;
+}
+
+mxfp4_status check_out(const void* p) {
+  if (p == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (!aligned16(p)) return MXFP4_ERR_MISALIGNED;
+  return MXFP4_OK;
+}
+
+#define MXFP4_TRY(expr)                      \
+  do {                                       \
+    mxfp4_status _s = (expr);                \
+    if (_s != MXFP4_OK) return _s;           \
+  } while (0)
+
+// Row-wise cast of an internal operand into the workspace.
+struct QuantView {
+  uint8_t* q;
+  uint8_t* sf;
+};
+
+QuantView carve(uint8_t*& cursor, int64_t rows, int64_t cols) {
+  QuantView v;
+  v.q = cursor;
+  cursor += align256(static_cast<size_t>(rows) * static_cast<size_t>(cols / 2));
+  v.sf = cursor;
+  cursor += align256(tile_scale_bytes(rows, cols));
+  return v;
+}
+
+size_t carve_bytes(int64_t rows, int64_t cols) {
+  return align256(static_cast<size_t>(rows) * static_cast<size_t>(cols / 2)) +
+         align256(tile_scale_bytes(rows, cols));
+}
+
+mxfp4_status gemm_checked(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
+                          const uint8_t* b_sf, uint16_t* c, int64_t M, int64_t N, int64_t K,
+                          int64_t ldc, cudaStream_t s) {
+  GemmArgs g{a, a_sf, b, b_sf, c, M, N, K, ldc};
+  cudaError_t e = mxfp4::launch_gemm(g, s);
+  if (e == cudaErrorInvalidValue) return MXFP4_ERR_INVALID_ARG;
+  return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int mxfp4_abi_version(void) { return 1; }
+
+const char* mxfp4_status_string(int status) {
+  switch (status) {
+    case MXFP4_OK: return "MXFP4_OK";
+    case MXFP4_ERR_INVALID_ARG: return "MXFP4_ERR_INVALID_ARG";
+    case MXFP4_ERR_MISALIGNED: return "MXFP4_ERR_MISALIGNED";
+    case MXFP4_ERR_UNSUPPORTED_DEVICE: return "MXFP4_ERR_UNSUPPORTED_DEVICE";
+    case MXFP4_ERR_WORKSPACE: return "MXFP4_ERR_WORKSPACE";
+    case MXFP4_ERR_CUDA: return "MXFP4_ERR_CUDA";
+    case MXFP4_ERR_TIMEOUT: return "MXFP4_ERR_TIMEOUT";
+    case MXFP4_ERR_NOT_IMPLEMENTED: return "MXFP4_ERR_NOT_IMPLEMENTED";
+    default: return "MXFP4_UNKNOWN_STATUS";
+  }
+}
+
+size_t mxfp4_codes_bytes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0) return 0;
+  return static_cast<size_t>(rows) * static_cast<size_t>(cols / 2);
+}
+
+size_t mxfp4_scales_bytes(int64_t rows, int64_t cols, uint32_t flags) {
+  if (rows < 0 || cols < 0) return 0;
+  if (flags & MXFP4_SCALE_LINEAR) return static_cast<size_t>(rows) * static_cast<size_t>(cols / 32);
+  return tile_scale_bytes(rows, cols);
+}
+
+mxfp4_status mxfp4_cast(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, uint8_t* q,
+                        uint8_t* sf, uint32_t flags, void* stream) {
+  if (flags & ~(MXFP4_HADAMARD_ROW | MXFP4_SCALE_LINEAR)) return MXFP4_ERR_INVALID_ARG;
+  MXFP4_TRY(check_bf16_in(x, rows, cols, ldx));
+  if (rows == 0 || cols == 0) return MXFP4_OK;
+  MXFP4_TRY(check_out(q));
+  MXFP4_TRY(check_out(sf));
+  MXFP4_TRY(check_device());
+  CastArgs a{x, rows, cols, ldx, q, sf, nullptr, nullptr, flags};
+  return from_cuda(mxfp4::launch_cast(a, static_cast<cudaStream_t>(stream)));
+}
+
+mxfp4_status mxfp4_cast_dual(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
+                             uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col,
+                             uint32_t flags, void* stream) {
+  if (flags & ~(MXFP4_HADAMARD_ROW | MXFP4_HADAMARD_COL | MXFP4_SCALE_LINEAR))
+    return MXFP4_ERR_INVALID_ARG;
+  MXFP4_TRY(check_bf16_in(x, rows, cols, ldx));
+  if (rows % 32 != 0) return MXFP4_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return MXFP4_OK;
+  MXFP4_TRY(check_out(q_row));
+  MXFP4_TRY(check_out(sf_row));
+  MXFP4_TRY(check_out(q_col));
+  MXFP4_TRY(check_out(sf_col));
+  MXFP4_TRY(check_device());
+  CastArgs a{x, rows, cols, ldx, q_row, sf_row, q_col, sf_col, flags};
+  return from_cuda(mxfp4::launch_cast(a, static_cast<cudaStream_t>(stream)));
+}
+
+mxfp4_status gemm_fp4(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, const uint8_t* b_sf,
+                      uint16_t* c, int64_t M, int64_t N, int64_t K, int64_t ldc, void* stream) {
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return MXFP4_ERR_INVALID_ARG;
+  if (K % 32 != 0 || ldc < N) return MXFP4_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return MXFP4_OK;
+  MXFP4_TRY(check_out(c));
+  if (ldc % 8 != 0) return MXFP4_ERR_MISALIGNED;
+  if (K > 0) {
+    MXFP4_TRY(check_out(a));
+    MXFP4_TRY(check_out(a_sf));
+    MXFP4_TRY(check_out(b));
+    MXFP4_TRY(check_out(b_sf));
+  }
+  MXFP4_TRY(check_device());
+  return gemm_checked(a, a_sf, b, b_sf, c, M, N, K, ldc, static_cast<cudaStream_t>(stream));
+}
+
+size_t mxfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0) return 0;
+  switch (op) {
+    case MXFP4_OP_FWD: return carve_bytes(M, K) + carve_bytes(N, K);    // row(X), row(W)
+    case MXFP4_OP_DGRAD: return carve_bytes(M, N) + carve_bytes(K, N);  // row(dY), col(W)
+    case MXFP4_OP_WGRAD: return carve_bytes(N, M) + carve_bytes(K, M);  // col(dY), col(X)
+    default: return 0;
+  }
+}
+
+mxfp4_status gemm_fp4_bf16_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y, int64_t M,
+                               int64_t N, int64_t K, void* ws, size_t ws_bytes, void* stream) {
+  MXFP4_TRY(check_bf16_in(x, M, K, K));
+  MXFP4_TRY(check_bf16_in(w, N, K, K));
+  if (M == 0 || N == 0) return MXFP4_OK;
+  MXFP4_TRY(check_out(y));
+  if (N % 8 != 0) return MXFP4_ERR_MISALIGNED;
+  if (ws == nullptr || ws_bytes < mxfp4_workspace_bytes(MXFP4_OP_FWD, M, N, K) || !aligned16(ws))
+    return MXFP4_ERR_WORKSPACE;
+  MXFP4_TRY(check_device());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return from_cuda(mxfp4::launch_fill_zero_bf16(y, M, N, N, s));
+  uint8_t* cur = static_cast<uint8_t*>(ws);
+  QuantView qx = carve(cur, M, K), qw = carve(cur, N, K);
+  CastArgs cx{x, M, K, K, qx.q, qx.sf, nullptr, nullptr, 0};
+  CastArgs cw{w, N, K, K, qw.q, qw.sf, nullptr, nullptr, 0};
+  MXFP4_TRY(from_cuda(mxfp4::launch_cast(cx, s)));
+  MXFP4_TRY(from_cuda(mxfp4::launch_cast(cw, s)));
+  return gemm_checked(qx.q, qx.sf, qw.q, qw.sf, y, M, N, K, N, s);
+}
+
+mxfp4_status gemm_fp4_bf16_dgrad(const uint16_t* dy, const uint16_t* w, uint16_t* dx, int64_t M,
+                                 int64_t N, int64_t K, void* ws, size_t ws_bytes, void* stream) {
+  MXFP4_TRY(check_bf16_in(dy, M, N, N));
+  MXFP4_TRY(check_bf16_in(w, N, K, K));
+  if (N % 32 != 0) return MXFP4_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return MXFP4_OK;
+  MXFP4_TRY(check_out(dx));
+  if (ws == nullptr || ws_bytes < mxfp4_workspace_bytes(MXFP4_OP_DGRAD, M, N, K) || !aligned16(ws))
+    return MXFP4_ERR_WORKSPACE;
+  MXFP4_TRY(check_device());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0) return from_cuda(mxfp4::launch_fill_zero_bf16(dx, M, K, K, s));
+  uint8_t* cur = static_cast<uint8_t*>(ws);
+  QuantView qdy = carve(cur, M, N), qwt = carve(cur, K, N);
+  CastArgs cdy{dy, M, N, N, qdy.q, qdy.sf, nullptr, nullptr, 0};
+  CastArgs cw{w, N, K, K, nullptr, nullptr, qwt.q, qwt.sf, 0};  // W^T, quantized along N
+  MXFP4_TRY(from_cuda(mxfp4::launch_cast(cdy, s)));
+  MXFP4_TRY(from_cuda(mxfp4::launch_cast(cw, s)));
+  return gemm_checked(qdy.q, qdy.sf, qwt.q, qwt.sf, dx, M, K, N, K, s);
+}
+
+mxfp4_status gemm_fp4_bf16_wgrad(const uint16_t* dy, const uint16_t* x, uint16_t* dw, int64_t M,
+                                 int64_t N, int64_t K, uint32_t flags, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  if (flags & ~MXFP4_HADAMARD_COL) return MXFP4_ERR_INVALID_ARG;
+  MXFP4_TRY(check_bf16_in(dy, M, N, N));
+  MXFP4_TRY(check_bf16_in(x, M, K, K));
+  if (M % 32 != 0) return MXFP4_ERR_INVALID_ARG;
+  if (N == 0 || K == 0) return MXFP4_OK;
+  MXFP4_TRY(check_out(dw));
+  if (ws == nullptr || ws_bytes < mxfp4_workspace_bytes(MXFP4_OP_WGRAD, M, N, K) || !aligned16(ws))
+    return MXFP4_ERR_WORKSPACE;
+  MXFP4_TRY(check_device());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M == 0) return from_cuda(mxfp4::launch_fill_zero_bf16(dw, N, K, K, s));
+  uint8_t* cur = static_cast<uint8_t*>(ws);
+  QuantView qdyt = carve(cur, N, M), qxt = carve(cur, K, M);
+  const uint32_t cf = (flags & MXFP4_HADAMARD_COL) ? mxfp4::kFlagHadamardCol : 0u;
+  CastArgs cdy{dy, M, N, N, nullptr, nullptr, qdyt.q, qdyt.sf, cf};  // dY^T along M
+  CastArgs cx{x, M, K, K, nullptr, nullptr, qxt.q, qxt.sf, cf};      // X^T along M
+  MXFP4_TRY(from_cuda(mxfp4::launch_cast(cdy, s)));
+  MXFP4_TRY(from_cuda(mxfp4::launch_cast(cx, s)));
+  return gemm_checked(qdyt.q, qdyt.sf, qxt.q, qxt.sf, dw, N, K, M, K, s);
+}
+
+mxfp4_status mxfp4_device_status(int reset, int* out_status) {
+  if (out_status == nullptr) return MXFP4_ERR_INVALID_ARG;
+  int v = 0;
+  if (mxfp4::read_device_status(&v, reset != 0) != cudaSuccess) return MXFP4_ERR_CUDA;
+  *out_status = v;
+  return MXFP4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,44 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mxfp4 {
+
+constexpr uint32_t kFlagHadamardRow = 1u;
+constexpr uint32_t kFlagHadamardCol = 2u;
+constexpr uint32_t kFlagScaleLinear = 4u;
+
+struct CastArgs {
+  const uint16_t* x;  // bf16 bits [rows, cols], pitch ldx
+  int64_t rows, cols, ldx;
+  uint8_t* q_row;   // [rows, cols/2] or null (no row-wise output)
+  uint8_t* sf_row;  // scales of the row-wise output
+  uint8_t* q_col;   // [cols, rows/2] or null (no column-wise output)
+  uint8_t* sf_col;  // scales of the column-wise output
+  uint32_t flags;
+};
+
+// One launch over 128 x 128 tiles of x; writes whichever outputs are non-null.
+cudaError_t launch_cast(const CastArgs& args, cudaStream_t stream);
+
+struct GemmArgs {
+  const uint8_t* a;     // codes [M, K/2]
+  const uint8_t* a_sf;  // tiled scales, M rows x K/32 blocks
+  const uint8_t* b;     // codes [N, K/2]
+  const uint8_t* b_sf;  // tiled scales, N rows x K/32 blocks
+  uint16_t* c;          // bf16 [M, N], pitch ldc
+  int64_t M, N, K, ldc;
+};
+
+cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
+
+// Reads (and optionally clears) the GEMM's device status word.  Synchronous.
+cudaError_t read_device_status(int* value, bool reset);
+
+// Zero-fill of a bf16 matrix (used when K == 0).
+cudaError_t launch_fill_zero_bf16(uint16_t* c, int64_t M, int64_t N, int64_t ldc,
+                                  cudaStream_t stream);
+
+}  // namespace mxfp4

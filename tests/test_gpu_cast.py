@@ -1,0 +1,140 @@
+"""GPU parity of the MXFP4 cast kernels against the oracle: codes and scales
+must match bit for bit (jax-aiter README, "Supported ops", MXFP4 Cast row:
+CastMxfp4JA row-wise, CastMxfp4DualJA row + transposed; "Quick start": grad
+cast with a Hadamard transform)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantization_mxfp4_cast_gb300 import synth
+from tests.test_oracle_pins import GOLDEN_BLOCKS, bf16_bits as golden_bits
+from tests.util import bf16_bits, build_library
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def m():
+    build_library()
+    import quantization_mxfp4_cast_gb300 as mod
+    return mod
+
+
+def tile_to_lin(sf_gpu, rows, cols):
+    return oracle.sf_tile_to_linear(sf_gpu.cpu().numpy(), rows, cols // 32)
+
+
+def check_row(m, x, hadamard, linear):
+    q, sf = m.mxfp4_cast(x.cuda(), hadamard=hadamard, linear_scales=linear)
+    torch.cuda.synchronize()
+    codes, scales = oracle.cast_rows(bf16_bits(x), hadamard=hadamard)
+    R, C = x.shape
+    got_sf = sf.cpu().numpy().reshape(R, C // 32) if linear else tile_to_lin(sf, R, C)
+    assert np.array_equal(got_sf, scales), "scales differ"
+    assert np.array_equal(q.cpu().numpy(), codes), "codes differ"
+    if not linear:  # padding bytes of the tiled layout are written as zero
+        full = oracle.sf_linear_to_tile(scales)
+        assert np.array_equal(sf.cpu().numpy(), full)
+
+
+def check_dual(m, x, had_row, had_col, linear):
+    qr, sr, qc, sc = m.mxfp4_cast_dual(x.cuda(), hadamard_row=had_row, hadamard_col=had_col,
+                                       linear_scales=linear)
+    torch.cuda.synchronize()
+    xb = bf16_bits(x)
+    R, C = x.shape
+    cr, srr = oracle.cast_rows(xb, hadamard=had_row)
+    cc, scc = oracle.cast_cols(xb, hadamard=had_col)
+    if linear:
+        assert np.array_equal(sr.cpu().numpy().reshape(R, C // 32), srr)
+        assert np.array_equal(sc.cpu().numpy().reshape(C, R // 32), scc)
+    else:
+        assert np.array_equal(sr.cpu().numpy(), oracle.sf_linear_to_tile(srr))
+        assert np.array_equal(sc.cpu().numpy(), oracle.sf_linear_to_tile(scc))
+    assert np.array_equal(qr.cpu().numpy(), cr)
+    assert np.array_equal(qc.cpu().numpy(), cc)
+
+
+SHAPES = [(256, 512), (128, 128), (96, 160), (1, 32), (300, 224), (640, 384)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("hadamard", [False, True])
+@pytest.mark.parametrize("linear", [False, True])
+def test_row_cast_parity(m, shape, hadamard, linear):
+    x = synth.with_outliers(synth.normal_bf16(shape, 1.0, seed=shape[0] + shape[1]), frac=0.01)
+    check_row(m, x, hadamard, linear)
+
+
+DUAL_SHAPES = [(256, 512), (128, 128), (96, 160), (32, 32), (320, 224), (640, 384)]
+
+
+@pytest.mark.parametrize("shape", DUAL_SHAPES)
+@pytest.mark.parametrize("had", [(False, False), (True, True), (False, True)])
+@pytest.mark.parametrize("linear", [False, True])
+def test_dual_cast_parity(m, shape, had, linear):
+    x = synth.with_outliers(synth.normal_bf16(shape, 1.0, seed=7 * shape[0] + shape[1]), frac=0.01)
+    check_dual(m, x, had[0], had[1], linear)
+
+
+def test_golden_blocks_on_gpu(m):
+    for blk in GOLDEN_BLOCKS:
+        bits = golden_bits(blk["x"]).reshape(1, 32)
+        x = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
+        q, sf = m.mxfp4_cast(x.cuda(), hadamard=blk["hadamard"], linear_scales=True)
+        torch.cuda.synchronize()
+        assert sf.cpu().numpy()[0] == blk["scale"], blk["name"]
+        assert q.cpu().numpy()[0].tolist() == blk["codes"], blk["name"]
+        # the same block as a column (32 rows x 1 column, padded to 32 columns)
+        xc = torch.zeros(32, 32, dtype=torch.bfloat16)
+        xc[:, 0] = x[0]
+        _, _, qc, sc = m.mxfp4_cast_dual(xc.cuda(), hadamard_col=blk["hadamard"], linear_scales=True)
+        torch.cuda.synchronize()
+        assert sc.cpu().numpy()[0] == blk["scale"], blk["name"]
+        assert qc.cpu().numpy()[0].tolist() == blk["codes"], blk["name"]
+
+
+@pytest.mark.parametrize("hadamard", [False, True])
+def test_exhaustive_bf16_patterns(m, hadamard):
+    # every one of the 65536 bf16 bit patterns, in natural order and in four
+    # seeded permutations, as blocks of 32 -- both directions
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    arrs = [pats] + [np.random.default_rng(s).permutation(pats) for s in range(4)]
+    bits = np.concatenate(arrs).reshape(-1, 256)  # 1280 x 256
+    x = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
+    check_dual(m, x, hadamard, hadamard, linear=False)
+
+
+def test_full_size_cast_config(m):
+    # activations [8192, 4096] ~ N(0,1) with 0.1% x50 outliers, dual, Hadamard off and on
+    x = synth.cast_input()
+    for had in (False, True):
+        check_dual(m, x, had, had, linear=False)
+
+
+def test_side_stream_ordering(m):
+    # work queued ahead on a side stream must finish before the cast reads x
+    s = torch.cuda.Stream()
+    ballast = torch.randn(4096, 4096, device="cuda")
+    x_host = synth.normal_bf16((2048, 1024), 1.0, seed=21)
+    x = torch.zeros(2048, 1024, dtype=torch.bfloat16, device="cuda")
+    with torch.cuda.stream(s):
+        for _ in range(8):
+            ballast = ballast @ ballast * 1e-3
+        x.copy_(x_host.cuda(non_blocking=False))
+        q, sf = m.mxfp4_cast(x, stream=s)
+    s.synchronize()
+    codes, scales = oracle.cast_rows(bf16_bits(x_host))
+    assert np.array_equal(q.cpu().numpy(), codes)
+    assert np.array_equal(tile_to_lin(sf, 2048, 1024), scales)
+
+
+def test_pitched_input(m):
+    big = synth.normal_bf16((192, 320), 1.0, seed=33).cuda()
+    view = big[:, 32:288]  # ldx = 320, 16-byte aligned start
+    q, sf = m.mxfp4_cast(view)
+    torch.cuda.synchronize()
+    codes, scales = oracle.cast_rows(bf16_bits(view.contiguous()))
+    assert np.array_equal(q.cpu().numpy(), codes)
+    assert np.array_equal(tile_to_lin(sf, 192, 256), scales)

@@ -1,0 +1,200 @@
+"""GPU parity of the block-scaled MXFP4 GEMM (tcgen05 kind::mxf4) against the
+fp64 oracle: |gpu - oracle| <= 2^-8 |oracle| + 1e-3 rms(oracle) elementwise.
+
+Method: jax-aiter README, "Supported ops" rows "FP4 GEMM (low-level)"
+(gemm_fp4 on pre-quantized fp4x2 + e8m0 operands) and "FP4 GEMM (training)"
+(A[M,K] . B[N,K]^T, BF16 in/out, FP4 forward, dA and dB; grad_out cast with a
+Hadamard transform)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantization_mxfp4_cast_gb300 import synth
+from tests.util import bf16_bits, build_library, gemm_tolerance_ok
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def m():
+    build_library()
+    import quantization_mxfp4_cast_gb300 as mod
+    return mod
+
+
+def to_dev_u8(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def run_gemm_fp4(m, ca, sa, cb, sb, M, N, K):
+    c = m.gemm_fp4(to_dev_u8(ca), to_dev_u8(oracle.sf_linear_to_tile(sa)), to_dev_u8(cb),
+                   to_dev_u8(oracle.sf_linear_to_tile(sb)), M, N, K)
+    torch.cuda.synchronize()
+    return c.float().cpu().numpy().astype(np.float64)
+
+
+def assert_close(gpu, ref, what=""):
+    ok, excess = gemm_tolerance_ok(gpu, ref)
+    assert ok, f"{what}: worst excess over tolerance {excess:.3e}"
+
+
+GEMM_SHAPES = [(256, 256, 512), (128, 256, 256), (200, 296, 320), (1, 8, 32), (384, 640, 1056),
+               (130, 264, 96), (512, 1024, 2048), (64, 512, 160)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+def test_gemm_fp4_on_oracle_operands(m, M, N, K):
+    xa = synth.with_outliers(synth.normal_bf16((M, K), 1.0, seed=M + K), frac=0.01)
+    xb = synth.normal_bf16((N, K), 0.02, seed=N + 3 * K)
+    ca, sa = oracle.cast_rows(bf16_bits(xa))
+    cb, sb = oracle.cast_rows(bf16_bits(xb))
+    ref = oracle.gemm_mxfp4(ca, sa, cb, sb, nthreads=8)
+    assert_close(run_gemm_fp4(m, ca, sa, cb, sb, M, N, K), ref, f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (160, 136, 384)])
+def test_gemm_fp4_random_codes_and_scales(m, M, N, K):
+    # every code value and a spread of scales, independent of the cast
+    rng = np.random.default_rng(M * N + K)
+    ca = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    cb = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sa = rng.integers(0x70, 0x8F, size=(M, K // 32), dtype=np.uint8)
+    sb = rng.integers(0x70, 0x8F, size=(N, K // 32), dtype=np.uint8)
+    ref = oracle.gemm_mxfp4(ca, sa, cb, sb, nthreads=8)
+    assert_close(run_gemm_fp4(m, ca, sa, cb, sb, M, N, K), ref)
+
+
+def test_gemm_fp4_one_hot_scales(m):
+    # all codes 1.0; one scale byte raised per operand: isolates the scale
+    # addressing (row, block) of both operands exactly
+    M, N, K = 256, 512, 512
+    ca = np.full((M, K // 2), 0x22, dtype=np.uint8)
+    cb = np.full((N, K // 2), 0x22, dtype=np.uint8)
+    for (ra, ka, rb, kb) in [(0, 0, 0, 0), (37, 5, 300, 11), (200, 15, 511, 3), (129, 8, 130, 9)]:
+        sa = np.full((M, K // 32), 0x7F, dtype=np.uint8)
+        sb = np.full((N, K // 32), 0x7F, dtype=np.uint8)
+        sa[ra, ka] = 0x81
+        sb[rb, kb] = 0x80
+        ref = oracle.gemm_mxfp4(ca, sa, cb, sb, nthreads=8)
+        got = run_gemm_fp4(m, ca, sa, cb, sb, M, N, K)
+        assert np.array_equal(got, ref), (ra, ka, rb, kb)
+
+
+def test_tiny_forward_config(m):
+    a, b = synth.tiny()
+    y = m.gemm_fp4_bf16_fwd(a.cuda(), b.cuda())
+    torch.cuda.synchronize()
+    ca, sa = oracle.cast_rows(bf16_bits(a))
+    cb, sb = oracle.cast_rows(bf16_bits(b))
+    ref = oracle.gemm_mxfp4(ca, sa, cb, sb, nthreads=8)
+    assert_close(y.float().cpu().numpy(), ref, "tiny fwd")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 384, 320), (96, 64, 128), (320, 160, 224)])
+def test_dgrad(m, M, N, K):
+    dy = synth.normal_bf16((M, N), 1e-3, seed=3)
+    w = synth.normal_bf16((N, K), 0.02, seed=2)
+    dx = m.gemm_fp4_bf16_dgrad(dy.cuda(), w.cuda())
+    torch.cuda.synchronize()
+    ca, sa = oracle.cast_rows(bf16_bits(dy))
+    cb, sb = oracle.cast_cols(bf16_bits(w))
+    ref = oracle.gemm_mxfp4(ca, sa, cb, sb, nthreads=8)
+    assert_close(dx.float().cpu().numpy(), ref, "dgrad")
+
+
+@pytest.mark.parametrize("hadamard", [True, False])
+@pytest.mark.parametrize("M,N,K", [(256, 384, 320), (96, 64, 128), (320, 160, 224)])
+def test_wgrad(m, M, N, K, hadamard):
+    dy = synth.normal_bf16((M, N), 1e-3, seed=3)
+    x = synth.normal_bf16((M, K), 1.0, seed=1)
+    dw = m.gemm_fp4_bf16_wgrad(dy.cuda(), x.cuda(), hadamard=hadamard)
+    torch.cuda.synchronize()
+    ca, sa = oracle.cast_cols(bf16_bits(dy), hadamard=hadamard)
+    cb, sb = oracle.cast_cols(bf16_bits(x), hadamard=hadamard)
+    ref = oracle.gemm_mxfp4(ca, sa, cb, sb, nthreads=8)
+    assert_close(dw.float().cpu().numpy(), ref, "wgrad")
+
+
+def test_k_zero_and_empty(m):
+    c = torch.full((8, 16), 7.0, dtype=torch.bfloat16, device="cuda")
+    dummy = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    m.gemm_fp4(dummy, dummy, dummy, dummy, 8, 16, 0, c=c)
+    torch.cuda.synchronize()
+    assert torch.all(c == 0)
+    e = torch.empty(0, 16, dtype=torch.bfloat16, device="cuda")
+    m.gemm_fp4(dummy, dummy, dummy, dummy, 0, 16, 64, c=e)
+
+
+def test_deterministic_and_side_stream(m):
+    M, N, K = 1024, 2048, 4096
+    x = synth.normal_bf16((M, K), 1.0, seed=1)
+    w = synth.normal_bf16((N, K), 0.02, seed=2)
+    y0 = m.gemm_fp4_bf16_fwd(x.cuda(), w.cuda())
+    s = torch.cuda.Stream()
+    ballast = torch.randn(8192, 8192, device="cuda")
+    xd = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
+    with torch.cuda.stream(s):
+        for _ in range(4):
+            ballast = ballast @ ballast * 1e-4
+        xd.copy_(x.cuda())
+        y1 = m.gemm_fp4_bf16_fwd(xd, w.cuda(), stream=s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1)
+    assert m.device_status() == 0
+
+
+def sample_idx(n, k, seed):
+    rng = np.random.default_rng(seed)
+    idx = rng.choice(n, size=min(k, n), replace=False)
+    idx[:2] = [0, n - 1] if n > 1 else [0, 0]
+    return np.unique(idx)
+
+
+def check_sampled_fwd(m, x, w, y, seed):
+    M, K = x.shape
+    N = w.shape[0]
+    si, sj = sample_idx(M, 24, seed), sample_idx(N, 48, seed + 1)
+    ca, sa = oracle.cast_rows(bf16_bits(x[si]))
+    cb, sb = oracle.cast_rows(bf16_bits(w[sj]))
+    ref = oracle.gemm_mxfp4(ca, sa, cb, sb, nthreads=8)
+    got = y[torch.from_numpy(si).cuda()][:, torch.from_numpy(sj).cuda()].float().cpu().numpy()
+    assert_close(got, ref, "sampled fwd")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["llama8b_gate_up", "llama70b_qkv"])
+def test_full_size_forward_sampled(m, name):
+    M, N, K, xs = synth.LLAMA_SHAPES[name]
+    x, w, _ = synth.linear_layer(M, N, K, xs)
+    y = m.gemm_fp4_bf16_fwd(x.cuda(), w.cuda())
+    torch.cuda.synchronize()
+    check_sampled_fwd(m, x, w, y, seed=5)
+    assert m.device_status() == 0
+
+
+@pytest.mark.slow
+def test_full_size_down_proj_train_step_sampled(m):
+    # 8B down projection: X[8192,14336], W[4096,14336], dY[8192,4096], Hadamard on wgrad
+    M, N, K, xs = synth.LLAMA_SHAPES["llama8b_down"]
+    x, w, dy = synth.linear_layer(M, N, K, xs)
+    xd, wd, dyd = x.cuda(), w.cuda(), dy.cuda()
+    y = m.gemm_fp4_bf16_fwd(xd, wd)
+    dx = m.gemm_fp4_bf16_dgrad(dyd, wd)
+    dw = m.gemm_fp4_bf16_wgrad(dyd, xd, hadamard=True)
+    torch.cuda.synchronize()
+    check_sampled_fwd(m, x, w, y, seed=6)
+    si, sk = sample_idx(M, 16, 7), sample_idx(K, 48, 8)
+    ca, sa = oracle.cast_rows(bf16_bits(dy[si]))
+    cb, sb = oracle.cast_cols(bf16_bits(w[:, sk]))
+    ref = oracle.gemm_mxfp4(ca, sa, cb, sb, nthreads=8)
+    got = dx[torch.from_numpy(si).cuda()][:, torch.from_numpy(sk).cuda()].float().cpu().numpy()
+    assert_close(got, ref, "sampled dgrad")
+    sn, sk = sample_idx(N, 16, 9), sample_idx(K, 48, 10)
+    ca, sa = oracle.cast_cols(bf16_bits(dy[:, sn]), hadamard=True)
+    cb, sb = oracle.cast_cols(bf16_bits(x[:, sk]), hadamard=True)
+    ref = oracle.gemm_mxfp4(ca, sa, cb, sb, nthreads=8)
+    got = dw[torch.from_numpy(sn).cuda()][:, torch.from_numpy(sk).cuda()].float().cpu().numpy()
+    assert_close(got, ref, "sampled wgrad")
+    assert m.device_status() == 0
