@@ -6,18 +6,31 @@
 // (training)" (A[M,K] . B[N,K]^T with BF16 output; forward, dA and dB all
 // run through it).  The pages' kernels are AMD assembly for MI355X; this is an
 // independent design for GB300:
-//   * persistent CTAs (one per SM), tile 128 x 256 of C, K step 256;
-//   * warp 0 lane 0: TMA producer -- codes by cp.async.bulk.tensor with the
-//     128-byte swizzle (one 256-element K slab is exactly one 128-byte
-//     swizzle row), scales by plain bulk copies of whole 512-byte scale tiles
-//     (the cast writes scales in the tensor-memory copy layout, so no
-//     reshuffle is needed), into a 4-stage shared-memory ring;
-//   * warp 1 lane 0: tensor-core issuer -- tcgen05.cp moves each stage's
-//     scales into tensor memory, then four tcgen05.mma.kind::mxf4 (K = 64
-//     each, two UE8M0 scales per row per MMA) accumulate into a 128 x 256
-//     fp32 tensor-memory accumulator; tcgen05.commit releases the stage;
-//   * warps 2-5: epilogue -- tcgen05.ld of the accumulator (each warp its
-//     32-lane sub-partition), fp32 -> bf16 round-to-nearest-even, stores.
+//   * CTA pairs (clusters of 2 on neighbouring SMs) run tcgen05.mma with
+//     cta_group::2: one 256 x 256 output tile per pair, each SM holding 128
+//     rows of A and 128 of the 256 rows of B, so every SM streams 8 KiB of
+//     operands per 64-deep MMA step instead of 12 KiB;
+//   * persistent: one pair per two SMs walks the tiles in groups of 8 row
+//     tiles (L2 reuse of A and B across the concurrently running tiles);
+//   * warp 0: TMA producer in each CTA -- FP4 codes with the 128-byte swizzle
+//     (a 256-element K slab is one 128-byte swizzle row) and the 512-byte
+//     scale tiles, which the cast already writes in the tensor-memory copy
+//     layout, into a 5-stage shared-memory ring;
+//   * warps 2-5, in each CTA: scale stagers -- each takes one 32-lane quarter
+//     of tensor memory and writes the stage's A and B scales there with
+//     tcgen05.st (the layout the block-scaled MMA reads: lane i of every
+//     quarter, column j = scales of row 32j + i), so the scale traffic never
+//     sits on the MMA issue path (measured: staging by tcgen05.cp in front of
+//     each stage's MMAs halved the MMA rate, tcgen05.st by four warps costs
+//     ~50 cycles per stage off the tensor pipe);
+//   * warp 1 of the first CTA: tensor-core issuer -- four
+//     tcgen05.mma.kind::mxf4 per stage (K = 64, two UE8M0 scales per row each)
+//     update a 256 x 256 fp32 accumulator (128 lanes x 256 columns in each
+//     SM); tcgen05.commit multicasts the stage release to both CTAs.  Warp 1
+//     of the second CTA relays "scales staged" to the first CTA's barrier;
+//   * warps 6-13: epilogue -- each warp reads 32 lanes x 128 columns of the
+//     accumulator, frees tensor memory at once, then converts to bf16 (round
+//     to nearest even) and stores while the next tile's MMAs run.
 // M and N tails come from the TMA out-of-bounds zero fill plus masked stores;
 // a K tail (K % 64 == 32) reads zero codes past K.
 #include <algorithm>
@@ -33,47 +46,72 @@ __device__ int g_device_status = 0;
 
 namespace {
 
-constexpr int kBM = 128;
-constexpr int kBN = 256;
-constexpr int kBK = 256;              // elements per stage
-constexpr int kBKBytes = kBK / 2;     // 128 bytes = one swizzle row
-constexpr int kStages = 4;
-constexpr int kAStage = kBM * kBKBytes;          // 16 KiB
-constexpr int kBStage = kBN * kBKBytes;          // 32 KiB
-constexpr int kSfaStage = (kBM / 128) * 2 * 512;  // 1 row tile x 2 K tiles
-constexpr int kSfbStage = (kBN / 128) * 2 * 512;  // 2 row tiles x 2 K tiles
-constexpr int kThreads = 192;
+constexpr int kBM = 256;                // rows of C per CTA pair
+constexpr int kRowsPerCta = 128;        // rows of A (and of B) held by each CTA
+constexpr int kBN = 256;                // columns of C per tile
+constexpr int kBK = 256;                // K elements per stage
+constexpr int kBKBytes = kBK / 2;       // 128 bytes = one swizzle row
+constexpr int kStages = 5;
+constexpr int kAStage = kRowsPerCta * kBKBytes;  // 16 KiB
+constexpr int kBStage = kRowsPerCta * kBKBytes;  // 16 KiB
+constexpr int kSfaStage = 2 * 512;               // own 128-row tile x 2 K tiles
+constexpr int kSfbStage = 2 * 2 * 512;           // both 128-row tiles of B x 2 K tiles
+constexpr uint32_t kStageBytes = kAStage + kBStage + kSfaStage + kSfbStage;
+constexpr int kGroupM = 8;                        // raster group (pair row tiles)
+constexpr int kScaleWarps = 4;   // warps 2-5
+constexpr int kEpiWarps = 8;     // warps 6-13
+constexpr int kFirstEpiWarp = 2 + kScaleWarps;
+constexpr int kThreads = 32 * (2 + kScaleWarps + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;
 constexpr uint32_t kSfCol0 = kBN;
-// per stage: SFA 2 K tiles x 4 columns, SFB 2 K tiles x 2 row tiles x 4 columns
-constexpr uint32_t kSfaCols = 8;
-constexpr uint32_t kSfStageCols = kSfaCols + 16;
+constexpr uint32_t kSfaCols = 8;                  // 2 K tiles x 4 columns
+constexpr uint32_t kSfStageCols = kSfaCols + 16;  // + 2 K tiles x 2 row tiles x 4 columns
 static_assert(kSfCol0 + kStages * kSfStageCols <= kTmemCols, "tensor memory budget");
 
-constexpr int kRingBytes = kStages * (kAStage + kBStage + kSfaStage + kSfbStage);
-constexpr int kSmemBytes = kRingBytes + 256 + 1024;  // + barriers, + alignment slack
+constexpr int kRingBytes = kStages * static_cast<int>(kStageBytes);
+constexpr int kSmemBytes = kRingBytes + 512 + 1024;  // + barriers, + alignment slack
 
-// Instruction descriptor, kind::mxf4: A and B E2M1 (format 1) K-major, D fp32,
-// N >> 3 at bit 17, UE8M0 scales (bit 23), M >> 4 at bit 24.  The scale
-// factor ids (bits 4-5 for B, 29-30 for A) select which byte pair of the
-// 32-bit tensor-memory scale column an MMA reads.
+// Instruction descriptor, kind::mxf4: A and B E2M1 (format 1), both K-major,
+// fp32 accumulator, N >> 3 at bit 17, UE8M0 scales (bit 23), M >> 4 at bit
+// 24 (M = 256: the pair).  The scale-factor ids (bits 4-5 for B, 29-30 for A)
+// pick the byte pair of the 32-bit tensor-memory scale column an MMA reads.
 constexpr uint32_t kIdescBase = (1u << 7) | (1u << 10) | (uint32_t(kBN >> 3) << 17) | (1u << 23) |
                                 (uint32_t(kBM >> 4) << 24);
 
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32) {
   uint32_t out;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out) : "f"(__uint_as_float(hi_f32)),
-      "f"(__uint_as_float(lo_f32)));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
+      : "=r"(out)
+      : "f"(__uint_as_float(hi_f32)), "f"(__uint_as_float(lo_f32)));
   return out;
 }
 
+// Tile t -> (pair row tile, column tile): groups of kGroupM row tiles, column
+// tiles outer within a group, so concurrently running tiles share A and B.
+__device__ __forceinline__ void tile_coords(int t, int num_mt, int num_nt, int& mt, int& nt) {
+  const int per_group = kGroupM * num_nt;
+  const int g = t / per_group;
+  const int first = g * kGroupM;
+  const int gm = min(kGroupM, num_mt - first);
+  const int r = t - g * per_group;
+  mt = first + r % gm;
+  nt = r / gm;
+}
+
+struct PairGemmParams {
+  GemmArgs args;
+  int num_mt, num_nt, num_kt, ktiles128;
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_mxf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const GemmArgs args, int num_mt, int num_nt, int num_kt, int ktiles128,
-                     int b_rowtiles) {
+    gemm_mxf4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmSfa,
+                          const __grid_constant__ CUtensorMap tmSfb, const PairGemmParams p) {
   extern __shared__ uint8_t smem_raw[];
-  // 1024-byte alignment for the 128-byte-swizzled operand tiles.
+  // 1024-byte alignment for the 128-byte-swizzled operand tiles (same offset
+  // in both CTAs: identical kernels, identical static layout).
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   uint8_t* sA = smem;
@@ -82,63 +120,74 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sSfb = sSfa + kStages * kSfaStage;
   uint64_t* full = reinterpret_cast<uint64_t*>(sSfb + kStages * kSfbStage);
   uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;
+  uint64_t* sf_ready = empty + kStages;
+  uint64_t* acc_full = sf_ready + kStages;
   uint64_t* acc_empty = acc_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_cta_rank();  // 0 = the CTA that issues the MMAs
+  const bool leader = rank == 0;
+  const GemmArgs& args = p.args;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      // leader: its own four stagers + the peer's relay; peer: its own four
+      mbar_init(&sf_ready[s], leader ? kScaleWarps + 1 : kScaleWarps);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4 * 32);
+    mbar_init(acc_empty, 2 * kEpiWarps);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmSfa);
+    tma_prefetch_desc(&tmSfb);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialized before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int num_tiles = num_mt * num_nt;
+  const int num_tiles = p.num_mt * p.num_nt;
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int num_pairs = static_cast<int>(gridDim.x >> 1);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-        const int mt = t % num_mt, nt = t / num_mt;
-        const int nbt = min(2, b_rowtiles - nt * 2);
-        for (int kt = 0; kt < num_kt; ++kt) {
+      for (int t = pair; ok && t < num_tiles; t += num_pairs) {
+        int mt, nt;
+        tile_coords(t, p.num_mt, p.num_nt, mt, nt);
+        const int a_row = mt * kBM + static_cast<int>(rank) * kRowsPerCta;
+        const int b_row = nt * kBN + static_cast<int>(rank) * kRowsPerCta;
+        const int a_rt = a_row / 128;  // this CTA's scale row tile of A
+        for (int kt = 0; kt < p.num_kt; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_device_status)) {
             ok = false;
             break;
           }
           const int kg0 = kt * 2;
-          const uint32_t sf_bytes = uint32_t(min(2, ktiles128 - kg0)) * 512u;
-          mbar_arrive_expect_tx(&full[stage], kAStage + kBStage + sf_bytes * (1 + nbt));
-          tma_load_2d(sA + stage * kAStage, &tmA, &full[stage], kt * kBKBytes, mt * kBM);
-          tma_load_2d(sB + stage * kBStage, &tmB, &full[stage], kt * kBKBytes, nt * kBN);
-          bulk_load(sSfa + stage * kSfaStage,
-                    args.a_sf + (static_cast<int64_t>(mt) * ktiles128 + kg0) * 512, sf_bytes,
-                    &full[stage]);
-          for (int j = 0; j < nbt; ++j)
-            bulk_load(sSfb + stage * kSfbStage + j * 1024,
-                      args.b_sf + (static_cast<int64_t>(nt * 2 + j) * ktiles128 + kg0) * 512,
-                      sf_bytes, &full[stage]);
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          tma_load_2d(sA + stage * kAStage, &tmA, &full[stage], kt * kBKBytes, a_row);
+          tma_load_2d(sB + stage * kBStage, &tmB, &full[stage], kt * kBKBytes, b_row);
+          tma_load_2d(sSfa + stage * kSfaStage, &tmSfa, &full[stage], 0,
+                      (a_rt * p.ktiles128 + kg0) * 4);
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            tma_load_2d(sSfb + stage * kSfbStage + j * 1024, &tmSfb, &full[stage], 0,
+                        ((nt * 2 + j) * p.ktiles128 + kg0) * 4);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -147,95 +196,159 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0, acc_phase = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-        if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, &g_device_status)) break;
-        tc_fence_after();
-        for (int kt = 0; kt < num_kt; ++kt) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, &g_device_status)) {
-            ok = false;
-            break;
-          }
+    if (leader) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        bool ok = true;
+        for (int t = pair; ok && t < num_tiles; t += num_pairs) {
+          if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, &g_device_status)) break;
           tc_fence_after();
-          const int nkg = min(2, ktiles128 - kt * 2);
-          const uint32_t sf_col = tmem_base + kSfCol0 + stage * kSfStageCols;
-          const uint32_t sfa_addr = smem_u32(sSfa + stage * kSfaStage);
-          const uint32_t sfb_addr = smem_u32(sSfb + stage * kSfbStage);
-          for (int g = 0; g < nkg; ++g) {
-            tc_cp_32x128b_warpx4(sf_col + g * 4, make_smem_desc(sfa_addr + g * 512, 0, 128, 0));
+          for (int kt = 0; kt < p.num_kt; ++kt) {
+            if (!mbar_wait(&sf_ready[stage], phase, abort_flag, &g_device_status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sf_col = tmem_base + kSfCol0 + stage * kSfStageCols;
+            const uint32_t a_addr = smem_u32(sA + stage * kAStage);
+            const uint32_t b_addr = smem_u32(sB + stage * kBStage);
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-              tc_cp_32x128b_warpx4(sf_col + kSfaCols + g * 8 + j * 4,
-                                   make_smem_desc(sfb_addr + j * 1024 + g * 512, 0, 128, 0));
+            for (int ks = 0; ks < 4; ++ks) {
+              if (static_cast<int64_t>(kt) * kBK + ks * 64 >= args.K) break;
+              const uint32_t g = ks >> 1, sf_id = (ks & 1) * 2;
+              const uint64_t adesc = make_smem_desc(a_addr + ks * 32, 16, 1024, 2);
+              const uint64_t bdesc = make_smem_desc(b_addr + ks * 32, 16, 1024, 2);
+              const uint32_t idesc = kIdescBase | (sf_id << 4) | (sf_id << 29);
+              tc_mma_pair_mxf4(tmem_base + kAccCol, adesc, bdesc, idesc, sf_col + g * 4,
+                               sf_col + kSfaCols + g * 8, (kt | ks) != 0);
+            }
+            tc_commit_pair(&empty[stage], 0x3);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          const uint32_t a_addr = smem_u32(sA + stage * kAStage);
-          const uint32_t b_addr = smem_u32(sB + stage * kBStage);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            if (static_cast<int64_t>(kt) * kBK + ks * 64 >= args.K) break;
-            const uint32_t g = ks >> 1, sf_id = (ks & 1) * 2;
-            const uint64_t adesc = make_smem_desc(a_addr + ks * 32, 16, 1024, 2);
-            const uint64_t bdesc = make_smem_desc(b_addr + ks * 32, 16, 1024, 2);
-            const uint32_t idesc = kIdescBase | (sf_id << 4) | (sf_id << 29);
-            tc_mma_mxf4(tmem_base + kAccCol, adesc, bdesc, idesc, sf_col + g * 4,
-                        sf_col + kSfaCols + g * 8, (kt | ks) != 0);
-          }
-          tc_commit(&empty[stage]);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
+          if (!ok) break;
+          tc_commit_pair(acc_full, 0x3);
+          acc_phase ^= 1u;
+        }
+      }
+    } else {
+      // ------------------------------------------------------------ relay (second CTA)
+      if (lane == 0) {
+        const uint32_t leader_ready0 = map_to_cta(&sf_ready[0], 0);
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int t = pair; ok && t < num_tiles; t += num_pairs) {
+          for (int kt = 0; kt < p.num_kt; ++kt) {
+            if (!mbar_wait(&sf_ready[stage], phase, abort_flag, &g_device_status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_cluster(leader_ready0 + stage * 8u);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
-        if (!ok) break;
-        tc_commit(acc_full);
-        acc_phase ^= 1u;
+      }
+    }
+  } else if (warp < kFirstEpiWarp) {
+    // ------------------------------------------------------------ scale stagers (both CTAs)
+    // Quarter q of tensor memory (lanes 32q .. 32q+31); thread i writes lane
+    // 32q + i.  Shared-memory scale tiles hold row r's 4 block scales at byte
+    // (r % 32) * 16 + (r / 32) * 4, so lane i's 16 bytes of a tile are exactly
+    // the 4 columns (rows i, i+32, i+64, i+96) the MMA reads for that tile.
+    const int q = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    for (int t = pair; ok && t < num_tiles; t += num_pairs) {
+      for (int kt = 0; kt < p.num_kt; ++kt) {
+        if (!mbar_wait(&full[stage], phase, abort_flag, &g_device_status)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* sfa = sSfa + stage * kSfaStage + lane * 16;
+        const uint8_t* sfb = sSfb + stage * kSfbStage + lane * 16;
+        const uint4 a0 = lds128(sfa), a1 = lds128(sfa + 512);
+        const uint4 b00 = lds128(sfb), b10 = lds128(sfb + 1024);
+        const uint4 b01 = lds128(sfb + 512), b11 = lds128(sfb + 1536);
+        const uint32_t taddr = tmem_base + lane_base + kSfCol0 + stage * kSfStageCols;
+        // columns 0-7: A, K tiles 0 and 1; 8-15: B K tile 0 (row tiles 0, 1); 16-23: B K tile 1
+        tmem_st_32x32b_x8(taddr + 0, a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w);
+        tmem_st_32x32b_x8(taddr + 8, b00.x, b00.y, b00.z, b00.w, b10.x, b10.y, b10.z, b10.w);
+        tmem_st_32x32b_x8(taddr + 16, b01.x, b01.y, b01.z, b01.w, b11.x, b11.y, b11.z, b11.w);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_ready[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // the tensor-memory lane quarter this warp may read
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;                         // tensor-memory lane quarter this warp may read
+    const int h = (warp - kFirstEpiWarp) >> 2;      // which 128-column half of the tile
+    const uint32_t acc_empty_leader = map_to_cta(acc_empty, 0);
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-      const int mt = t % num_mt, nt = t / num_mt;
+    for (int t = pair; t < num_tiles; t += num_pairs) {
+      int mt, nt;
+      tile_coords(t, p.num_mt, p.num_nt, mt, nt);
       if (!mbar_wait(acc_full, acc_phase, abort_flag, &g_device_status)) break;
       tc_fence_after();
-      const int64_t row = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
-#pragma unroll 1
-      for (int ch = 0; ch < kBN / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + ch * 32, r);
+      // Two rounds of 64 columns: load, convert to bf16 pairs, store; tensor
+      // memory is released as soon as the last columns are in registers.
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + h * 128;
+      const int64_t row = static_cast<int64_t>(mt) * kBM + rank * kRowsPerCta + q * 32 + lane;
+      const int64_t col0 = static_cast<int64_t>(nt) * kBN + h * 128;
+      uint16_t* dst_row = args.c + row * args.ldc + col0;
+      const bool row_ok = row < args.M;
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32(taddr + c2 * 64, r0);
+        tmem_ld_32x32b_x32(taddr + c2 * 64 + 32, r1);
         tmem_ld_wait();
-        const int64_t col = static_cast<int64_t>(nt) * kBN + ch * 32;
-        if (row < args.M && col < args.N) {
-          uint32_t p[16];
+        if (c2 == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty_leader);  // accumulator free for the next tile
+        }
+        uint32_t pk[32];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) p[j] = pack_bf16x2(r[2 * j], r[2 * j + 1]);
-          uint16_t* dst = args.c + row * args.ldc + col;
-          if (col + 32 <= args.N) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
+        for (int j = 0; j < 16; ++j) {
+          pk[j] = pack_bf16x2(r0[2 * j], r0[2 * j + 1]);
+          pk[16 + j] = pack_bf16x2(r1[2 * j], r1[2 * j + 1]);
+        }
+        const int64_t n_left = args.N - (col0 + c2 * 64);  // columns of this round that exist
+        if (row_ok && n_left >= 64) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst_row + c2 * 64);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) d4[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
-          } else {
-            const int n_left = static_cast<int>(args.N - col);
-            for (int e = 0; e < n_left; ++e)
-              dst[e] = static_cast<uint16_t>((e & 1) ? (p[e >> 1] >> 16) : (p[e >> 1] & 0xFFFFu));
+          for (int j = 0; j < 8; ++j)
+            d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        } else if (row_ok && n_left > 0) {
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            if (e < n_left) dst_row[c2 * 64 + e] = static_cast<uint16_t>(pk[e >> 1] & 0xFFFFu);
+            if (e + 1 < n_left) dst_row[c2 * 64 + e + 1] = static_cast<uint16_t>(pk[e >> 1] >> 16);
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(acc_empty);
       acc_phase ^= 1u;
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // neither CTA leaves while its peer may still touch its barriers or memory
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -253,31 +366,57 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = [] {
-    void* p = nullptr;
+    void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
                                          &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<EncodeTiledFn>(p);
+      ptr = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(ptr);
   }();
   return fn;
 }
 
-// 2-D map over a [rows, K/2] byte matrix, boxes of box_rows x 128 bytes,
-// 128-byte swizzle, zero fill out of bounds.
-bool make_codes_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t k_bytes,
-                    uint32_t box_rows) {
+// 2-D byte matrix [rows, row_bytes] (pitch row_bytes), boxes of box_rows x
+// box_bytes, zero fill out of bounds.
+bool make_byte_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t row_bytes,
+                   uint32_t box_bytes, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(k_bytes), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(k_bytes)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBKBytes), box_rows};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  cuuint32_t box[2] = {box_bytes, box_rows};
   cuuint32_t estrides[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides,
-                  box, estrides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, estrides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Largest number of co-resident CTA pairs, per device (cached).
+int max_pairs(int dev) {
+  static int cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_mxf4_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    n = std::max(1, sms / 2);
+  }
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
 }
 
 }  // namespace
@@ -301,26 +440,44 @@ cudaError_t launch_fill_zero_bf16(uint16_t* c, int64_t M, int64_t N, int64_t ldc
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream) {
   if (args.M == 0 || args.N == 0) return cudaSuccess;
   if (args.K == 0) return launch_fill_zero_bf16(args.c, args.M, args.N, args.ldc, stream);
-  CUtensorMap tmA, tmB;
-  if (!make_codes_map(&tmA, args.a, args.M, args.K / 2, kBM) ||
-      !make_codes_map(&tmB, args.b, args.N, args.K / 2, kBN))
+  const int64_t ktiles128 = (args.K + 127) / 128;
+  const int64_t a_sf_rows = (args.M + 127) / 128 * ktiles128 * 4;  // 128-byte rows of the scale buffer
+  const int64_t b_sf_rows = (args.N + 127) / 128 * ktiles128 * 4;
+  CUtensorMap tmA, tmB, tmSfa, tmSfb;
+  if (!make_byte_map(&tmA, args.a, args.M, args.K / 2, kBKBytes, kRowsPerCta, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_byte_map(&tmB, args.b, args.N, args.K / 2, kBKBytes, kRowsPerCta, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_byte_map(&tmSfa, args.a_sf, a_sf_rows, 128, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_byte_map(&tmSfb, args.b_sf, b_sf_rows, 128, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  int dev = 0, sms = 0;
+  int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  e = cudaFuncSetAttribute(gemm_mxf4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(gemm_mxf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  PairGemmParams p;
+  p.args = args;
+  p.num_mt = static_cast<int>((args.M + kBM - 1) / kBM);
+  p.num_nt = static_cast<int>((args.N + kBN - 1) / kBN);
+  p.num_kt = static_cast<int>((args.K + kBK - 1) / kBK);
+  p.ktiles128 = static_cast<int>(ktiles128);
+  const int64_t tiles = static_cast<int64_t>(p.num_mt) * p.num_nt;
+  const int pairs = static_cast<int>(std::min<int64_t>(tiles, max_pairs(dev)));
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel, tmA, tmB, tmSfa, tmSfb, p);
   if (e != cudaSuccess) return e;
-  const int num_mt = static_cast<int>((args.M + kBM - 1) / kBM);
-  const int num_nt = static_cast<int>((args.N + kBN - 1) / kBN);
-  const int num_kt = static_cast<int>((args.K + kBK - 1) / kBK);
-  const int ktiles128 = static_cast<int>((args.K + 127) / 128);
-  const int b_rowtiles = static_cast<int>((args.N + 127) / 128);
-  const int64_t tiles = static_cast<int64_t>(num_mt) * num_nt;
-  const int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
-  gemm_mxf4_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, args, num_mt, num_nt, num_kt,
-                                                           ktiles128, b_rowtiles);
   return cudaGetLastError();
 }
 
