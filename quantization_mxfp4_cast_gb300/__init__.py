@@ -33,6 +33,7 @@ ABI_SYMBOLS = (
     "mxfp4_abi_version", "mxfp4_status_string", "mxfp4_codes_bytes", "mxfp4_scales_bytes",
     "mxfp4_cast", "mxfp4_cast_dual", "gemm_fp4", "mxfp4_workspace_bytes",
     "gemm_fp4_bf16_fwd", "gemm_fp4_bf16_dgrad", "gemm_fp4_bf16_wgrad", "mxfp4_device_status",
+    "gemm_fp4_bf16_fwd_noalloc",
 )
 
 _lib = None
@@ -69,6 +70,7 @@ def lib() -> ctypes.CDLL:
                 "gemm_fp4_bf16_dgrad": (I, [P, P, P, I64, I64, I64, P, SZ, P]),
                 "gemm_fp4_bf16_wgrad": (I, [P, P, P, I64, I64, I64, U32, P, SZ, P]),
                 "mxfp4_device_status": (I, [I, ctypes.POINTER(I)]),
+                "gemm_fp4_bf16_fwd_noalloc": (I, [P, P, P, I64, I64, I64, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -220,6 +222,26 @@ def gemm_fp4_bf16_wgrad(dy, x, hadamard: bool = True, dw=None, ws=None, stream=N
     _check(lib().gemm_fp4_bf16_wgrad(_ptr(dy), _ptr(x), _ptr(dw), M, N, K, flags, _ptr(ws), nb,
                                      _stream(stream)), "gemm_fp4_bf16_wgrad")
     return dw
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20  # MXFP4_NOALLOC_SCRATCH_BYTES
+
+
+def gemm_fp4_bf16_fwd_noalloc(x, w, y=None, stream=None):
+    """Y[M,N] = X[M,K] . W[N,K]^T like gemm_fp4_bf16_fwd, but for callers that
+    cannot allocate device memory: no workspace argument, the quantized operands
+    go to the library's own 32 MiB device array (shared by all calls; calls that
+    overlap on the GPU race).  Sizes needing more raise Mxfp4Error
+    (MXFP4_ERR_WORKSPACE).  Allocates y with torch only if it is not given."""
+    _bf16_2d(x, "x"), _bf16_2d(w, "w")
+    _need_cuda(x, w)
+    M, K = x.shape
+    N = w.shape[0]
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    _check(lib().gemm_fp4_bf16_fwd_noalloc(_ptr(x), _ptr(w), _ptr(y), M, N, K, _stream(stream)),
+           "gemm_fp4_bf16_fwd_noalloc")
+    return y
 
 
 def device_status(reset: bool = True) -> int:

@@ -15,7 +15,7 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libmxfp4.so")
-SOURCES = ["cast.cu", "gemm.cu", "api.cu"]
+SOURCES = ["cast.cu", "gemm.cu", "api.cu", "noalloc.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
