@@ -321,7 +321,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
@@ -352,9 +352,16 @@ def main():
         raise RuntimeError("device status word set during warm-up")
 
     # --------------------------------------------------------------- timed region (HBM-resident inputs)
+    # One step (6 launches through the C ABI) is captured once as a CUDA graph
+    # and replayed K times, so the host never starves the GPU between launches.
     n_launch = len(step.launches(stream))
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_launch)]
-           for _ in range(args.steps)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step.run(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+    stream.synchronize()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
     smi_index = int(visible[local]) if len(visible) > local and visible[local].isdigit() else local
@@ -363,8 +370,8 @@ def main():
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             t_start.record(stream)
-            for i in range(args.steps):
-                step.run(stream, evs[i])
+            for _ in range(args.steps):
+                graph.replay()
             t_end.record(stream)
         stream.synchronize()
         torch.cuda.synchronize()
@@ -372,13 +379,37 @@ def main():
     elapsed = max_over_ranks(t_start.elapsed_time(t_end) / 1e3, world, dev)
     if m.device_status() != 0:
         raise RuntimeError("device status word set in the timed region")
+    value = world * STEP_FLOPS * args.steps / elapsed / 1e12
+    ms_per_step = elapsed / args.steps * 1e3
+
+    # --------------------------------------------------------------- per-kernel times
+    # Eager launches with an event pair around each, all enqueued while the
+    # stream is held by a GPU sleep, so the events time back-to-back GPU work.
+    n_prof = min(args.steps, 20)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_launch)]
+           for _ in range(n_prof)]
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        step.run(stream)
+    stream.synchronize()
+    host_per_step = time.perf_counter() - t0
+    for attempt in range(3):
+        sleep_s = 0.005 + 2.0 * n_prof * host_per_step * (2 ** attempt)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(sleep_s * 2.2e9))
+            h0 = time.perf_counter()
+            for i in range(n_prof):
+                step.run(stream, evs[i])
+            host_enqueue = time.perf_counter() - h0
+        stream.synchronize()
+        if host_enqueue < sleep_s:
+            break
     kinds = [k for k, _ in step.launches(stream)]
-    per = [[evs[i][j][0].elapsed_time(evs[i][j][1]) / 1e3 for j in range(n_launch)] for i in range(args.steps)]
+    per = [[evs[i][j][0].elapsed_time(evs[i][j][1]) / 1e3 for j in range(n_launch)] for i in range(n_prof)]
     gemm_t = [sum(p[j] for j in range(n_launch) if kinds[j] == "gemm") for p in per]
     cast_t = [sum(p[j] for j in range(n_launch) if kinds[j] == "cast") for p in per]
     launch_mean = [statistics.mean(p[j] for p in per) for j in range(n_launch)]
-    value = world * STEP_FLOPS * args.steps / elapsed / 1e12
-    ms_per_step = elapsed / args.steps * 1e3
 
     peaks = load_peaks()
     fp4_peak = peaks["bf16"] * NOMINAL_FP4_OVER_BF16
@@ -444,6 +475,8 @@ def main():
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": n_launch * args.steps,
+            "timing": {"timed_region": "CUDA-graph replay of the captured step, K times, CUDA events on the launch stream",
+                       "per_kernel": f"{n_prof} eager steps enqueued behind a GPU sleep, an event pair per launch"},
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)

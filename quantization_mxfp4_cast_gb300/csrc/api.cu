@@ -8,6 +8,7 @@
 // activation cast + weight cast + GEMM; backward = gradient cast + dA GEMM,
 // plus the dB GEMM).
 #include <algorithm>
+#include <atomic>
 
 #include "../../include/mxfp4.h"
 #include "internal.h"
@@ -22,14 +23,22 @@ constexpr int64_t kMaxDim = int64_t(1) << 31;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The current device must be compute capability 10.3.  The answer per device
+// is cached (it cannot change within a process): 0 unknown, 1 yes, 2 no.
 mxfp4_status check_device() {
-  int dev = 0, major = 0, minor = 0;
+  static std::atomic<int> known[64];
+  int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MXFP4_ERR_CUDA;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return MXFP4_ERR_CUDA;
-  if (major != 10 || minor != 3) return MXFP4_ERR_UNSUPPORTED_DEVICE;
-  return MXFP4_OK;
+  int k = (dev >= 0 && dev < 64) ? known[dev].load(std::memory_order_relaxed) : 0;
+  if (k == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return MXFP4_ERR_CUDA;
+    k = (major == 10 && minor == 3) ? 1 : 2;
+    if (dev >= 0 && dev < 64) known[dev].store(k, std::memory_order_relaxed);
+  }
+  return k == 1 ? MXFP4_OK : MXFP4_ERR_UNSUPPORTED_DEVICE;
 }
 
 mxfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA; }

@@ -26,14 +26,19 @@
 //   * warp 1 of the first CTA: tensor-core issuer -- four
 //     tcgen05.mma.kind::mxf4 per stage (K = 64, two UE8M0 scales per row each)
 //     update a 256 x 256 fp32 accumulator (128 lanes x 256 columns in each
-//     SM); tcgen05.commit multicasts the stage release to both CTAs.  Warp 1
-//     of the second CTA relays "scales staged" to the first CTA's barrier;
+//     SM); tcgen05.commit multicasts the stage release to both CTAs.  The
+//     stagers of both CTAs report "stage ready" straight to the first CTA's
+//     barrier (their own data has landed by then), so no relay hop;
 //   * warps 6-13: epilogue -- each warp reads 32 lanes x 128 columns of the
-//     accumulator, frees tensor memory at once, then converts to bf16 (round
-//     to nearest even) and stores while the next tile's MMAs run.
-// M and N tails come from the TMA out-of-bounds zero fill plus masked stores;
-// a K tail (K % 64 == 32) reads zero codes past K.
+//     accumulator in two 64-column rounds, frees tensor memory after the
+//     second read, converts to bf16 (round to nearest even), writes the
+//     32 x 64 block into its own 128-byte-swizzled shared-memory buffer and
+//     hands it to a TMA store, so the global writes are whole-line and
+//     asynchronous while the next tile's MMAs run.
+// M and N tails come from the TMA out-of-bounds zero fill on loads and the
+// TMA clipping of stores; a K tail (K % 64 == 32) reads zero codes past K.
 #include <algorithm>
+#include <atomic>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -70,7 +75,8 @@ constexpr uint32_t kSfStageCols = kSfaCols + 16;  // + 2 K tiles x 2 row tiles x
 static_assert(kSfCol0 + kStages * kSfStageCols <= kTmemCols, "tensor memory budget");
 
 constexpr int kRingBytes = kStages * static_cast<int>(kStageBytes);
-constexpr int kSmemBytes = kRingBytes + 512 + 1024;  // + barriers, + alignment slack
+constexpr int kOutStageBytes = 32 * 64 * 2;  // per epilogue warp: 32 rows x 64 bf16 columns
+constexpr int kSmemBytes = kRingBytes + kEpiWarps * kOutStageBytes + 512 + 1024;
 
 // Instruction descriptor, kind::mxf4: A and B E2M1 (format 1), both K-major,
 // fp32 accumulator, N >> 3 at bit 17, UE8M0 scales (bit 23), M >> 4 at bit
@@ -108,7 +114,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_mxf4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSfa,
-                          const __grid_constant__ CUtensorMap tmSfb, const PairGemmParams p) {
+                          const __grid_constant__ CUtensorMap tmSfb,
+                          const __grid_constant__ CUtensorMap tmC, const PairGemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte-swizzled operand tiles (same offset
   // in both CTAs: identical kernels, identical static layout).
@@ -118,7 +125,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sB = sA + kStages * kAStage;
   uint8_t* sSfa = sB + kStages * kBStage;
   uint8_t* sSfb = sSfa + kStages * kSfaStage;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sSfb + kStages * kSfbStage);
+  uint8_t* sOut = sSfb + kStages * kSfbStage;  // epilogue staging, 1024-byte aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + kEpiWarps * kOutStageBytes);
   uint64_t* empty = full + kStages;
   uint64_t* sf_ready = empty + kStages;
   uint64_t* acc_full = sf_ready + kStages;
@@ -136,8 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      // leader: its own four stagers + the peer's relay; peer: its own four
-      mbar_init(&sf_ready[s], leader ? kScaleWarps + 1 : kScaleWarps);
+      // leader only: the four stager warps of each CTA arrive here
+      mbar_init(&sf_ready[s], 2 * kScaleWarps);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * kEpiWarps);
@@ -149,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmSfa);
     tma_prefetch_desc(&tmSfb);
+    tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, kTmemCols);
@@ -234,26 +243,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc_phase ^= 1u;
         }
       }
-    } else {
-      // ------------------------------------------------------------ relay (second CTA)
-      if (lane == 0) {
-        const uint32_t leader_ready0 = map_to_cta(&sf_ready[0], 0);
-        uint32_t stage = 0, phase = 0;
-        bool ok = true;
-        for (int t = pair; ok && t < num_tiles; t += num_pairs) {
-          for (int kt = 0; kt < p.num_kt; ++kt) {
-            if (!mbar_wait(&sf_ready[stage], phase, abort_flag, &g_device_status)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_cluster(leader_ready0 + stage * 8u);
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-        }
-      }
     }
   } else if (warp < kFirstEpiWarp) {
     // ------------------------------------------------------------ scale stagers (both CTAs)
@@ -263,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the 4 columns (rows i, i+32, i+64, i+96) the MMA reads for that tile.
     const int q = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t leader_ready0 = map_to_cta(&sf_ready[0], 0);
     uint32_t stage = 0, phase = 0;
     bool ok = true;
     for (int t = pair; ok && t < num_tiles; t += num_pairs) {
@@ -284,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sf_ready[stage]);
+        if (lane == 0) mbar_arrive_cluster(leader_ready0 + stage * 8u);  // the issuing CTA's barrier
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
@@ -296,19 +286,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                         // tensor-memory lane quarter this warp may read
     const int h = (warp - kFirstEpiWarp) >> 2;      // which 128-column half of the tile
     const uint32_t acc_empty_leader = map_to_cta(acc_empty, 0);
+    const uint32_t out_buf = smem_u32(sOut + (warp - kFirstEpiWarp) * kOutStageBytes);
     uint32_t acc_phase = 0;
     for (int t = pair; t < num_tiles; t += num_pairs) {
       int mt, nt;
       tile_coords(t, p.num_mt, p.num_nt, mt, nt);
       if (!mbar_wait(acc_full, acc_phase, abort_flag, &g_device_status)) break;
       tc_fence_after();
-      // Two rounds of 64 columns: load, convert to bf16 pairs, store; tensor
-      // memory is released as soon as the last columns are in registers.
+      // Two rounds of 64 columns: load, convert to bf16 pairs, stage, store;
+      // tensor memory is released as soon as the last columns are in registers.
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + h * 128;
-      const int64_t row = static_cast<int64_t>(mt) * kBM + rank * kRowsPerCta + q * 32 + lane;
-      const int64_t col0 = static_cast<int64_t>(nt) * kBN + h * 128;
-      uint16_t* dst_row = args.c + row * args.ldc + col0;
-      const bool row_ok = row < args.M;
+      const int32_t row0 = mt * kBM + static_cast<int32_t>(rank) * kRowsPerCta + q * 32;
+      const int32_t col0 = nt * kBN + h * 128;
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t r0[32], r1[32];
@@ -326,22 +315,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[j] = pack_bf16x2(r0[2 * j], r0[2 * j + 1]);
           pk[16 + j] = pack_bf16x2(r1[2 * j], r1[2 * j + 1]);
         }
-        const int64_t n_left = args.N - (col0 + c2 * 64);  // columns of this round that exist
-        if (row_ok && n_left >= 64) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst_row + c2 * 64);
+        // the previous store out of this buffer must have finished reading it
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+        // row `lane` of the block: eight 16-byte chunks, chunk j at j ^ (row % 8)
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-        } else if (row_ok && n_left > 0) {
-#pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            if (e < n_left) dst_row[c2 * 64 + e] = static_cast<uint16_t>(pk[e >> 1] & 0xFFFFu);
-            if (e + 1 < n_left) dst_row[c2 * 64 + e + 1] = static_cast<uint16_t>(pk[e >> 1] >> 16);
-          }
+        for (int j = 0; j < 8; ++j)
+          sts128(out_buf + lane * 128 + ((j ^ (lane & 7)) * 16), pk[4 * j], pk[4 * j + 1],
+                 pk[4 * j + 2], pk[4 * j + 3]);
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmC, sOut + (warp - kFirstEpiWarp) * kOutStageBytes, col0 + c2 * 64, row0);
+          bulk_commit_group();
         }
       }
       acc_phase ^= 1u;
     }
+    if (lane == 0) bulk_wait_group0();
   }
 
   tc_fence_before();
@@ -393,10 +384,36 @@ bool make_byte_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t 
   return r == CUDA_SUCCESS;
 }
 
+// Output map: bf16 [M, N] with row pitch ldc elements, boxes of 32 rows x 64
+// columns (128 bytes, 128-byte swizzle); stores clip at M and N.
+bool make_bf16_out_map(CUtensorMap* map, uint16_t* base, int64_t M, int64_t N, int64_t ldc) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estrides[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estrides,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Shared-memory opt-in of the kernel, once per device.
+cudaError_t prepare_kernel(int dev) {
+  static std::atomic<bool> done[64];
+  if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(gemm_mxf4_pair_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
+  return e;
+}
+
 // Largest number of co-resident CTA pairs, per device (cached).
 int max_pairs(int dev) {
-  static int cache[64] = {0};
-  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  static std::atomic<int> cache[64];
+  if (dev >= 0 && dev < 64 && cache[dev].load(std::memory_order_relaxed) > 0)
+    return cache[dev].load(std::memory_order_relaxed);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -415,7 +432,7 @@ int max_pairs(int dev) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     n = std::max(1, sms / 2);
   }
-  if (dev >= 0 && dev < 64) cache[dev] = n;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -449,11 +466,12 @@ cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream) {
       !make_byte_map(&tmSfa, args.a_sf, a_sf_rows, 128, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_byte_map(&tmSfb, args.b_sf, b_sf_rows, 128, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
+  CUtensorMap tmC;
+  if (!make_bf16_out_map(&tmC, args.c, args.M, args.N, args.ldc)) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(gemm_mxf4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes);
+  e = prepare_kernel(dev);
   if (e != cudaSuccess) return e;
   PairGemmParams p;
   p.args = args;
@@ -476,7 +494,7 @@ cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel, tmA, tmB, tmSfa, tmSfb, p);
+  e = cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel, tmA, tmB, tmSfa, tmSfb, tmC, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
