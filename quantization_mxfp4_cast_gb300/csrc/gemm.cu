@@ -350,29 +350,11 @@ __global__ void fill_zero_bf16_kernel(uint16_t* c, int64_t M, int64_t N, int64_t
     c[(i / N) * ldc + (i % N)] = 0;
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      ptr = nullptr;
-    return reinterpret_cast<EncodeTiledFn>(ptr);
-  }();
-  return fn;
-}
-
 // 2-D byte matrix [rows, row_bytes] (pitch row_bytes), boxes of box_rows x
 // box_bytes, zero fill out of bounds.
 bool make_byte_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t row_bytes,
                    uint32_t box_bytes, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
-  EncodeTiledFn fn = encode_fn();
+  EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
@@ -387,7 +369,7 @@ bool make_byte_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t 
 // Output map: bf16 [M, N] with row pitch ldc elements, boxes of 32 rows x 64
 // columns (128 bytes, 128-byte swizzle); stores clip at M and N.
 bool make_bf16_out_map(CUtensorMap* map, uint16_t* base, int64_t M, int64_t N, int64_t ldc) {
-  EncodeTiledFn fn = encode_fn();
+  EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * 2};
@@ -437,6 +419,33 @@ int max_pairs(int dev) {
 }
 
 }  // namespace
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      ptr = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+int* device_status_word() {
+  static std::atomic<int*> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  int* p = cache[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return nullptr;
+    p = static_cast<int*>(addr);
+    cache[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
 
 cudaError_t read_device_status(int* value, bool reset) {
   cudaError_t e = cudaMemcpyFromSymbol(value, g_device_status, sizeof(int));

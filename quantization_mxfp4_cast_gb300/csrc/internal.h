@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI (api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -34,7 +35,20 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
 
-// Reads (and optionally clears) the GEMM's device status word.  Synchronous.
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (so the library needs no link-time dependency on libcuda); null if missing.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+// Device address of the library's status word on the current device (looked
+// up once per device); null on failure.  Kernels with bounded waits record
+// MXFP4_ERR_TIMEOUT there.
+int* device_status_word();
+
+// Reads (and optionally clears) the device status word.  Synchronous.
 cudaError_t read_device_status(int* value, bool reset);
 
 // Zero-fill of a bf16 matrix (used when K == 0).
