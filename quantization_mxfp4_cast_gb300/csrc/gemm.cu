@@ -15,7 +15,9 @@
 //   * warp 0: TMA producer in each CTA -- FP4 codes with the 128-byte swizzle
 //     (a 256-element K slab is one 128-byte swizzle row) and the 512-byte
 //     scale tiles, which the cast already writes in the tensor-memory copy
-//     layout, into a 5-stage shared-memory ring;
+//     layout, into a 6-stage shared-memory ring (the measured
+//     stage round trip -- TMA from L2, staging, MMA, release -- is ~1.5 us,
+//     six 256 ns MMA stages cover it);
 //   * warps 2-5, in each CTA: scale stagers -- each takes one 32-lane quarter
 //     of tensor memory and writes the stage's A and B scales there with
 //     tcgen05.st (the layout the block-scaled MMA reads: lane i of every
@@ -30,11 +32,10 @@
 //     stagers of both CTAs report "stage ready" straight to the first CTA's
 //     barrier (their own data has landed by then), so no relay hop;
 //   * warps 6-13: epilogue -- each warp reads 32 lanes x 128 columns of the
-//     accumulator in two 64-column rounds, frees tensor memory after the
-//     second read, converts to bf16 (round to nearest even), writes the
-//     32 x 64 block into its own 128-byte-swizzled shared-memory buffer and
-//     hands it to a TMA store, so the global writes are whole-line and
-//     asynchronous while the next tile's MMAs run.
+//     accumulator into registers as bf16 pairs, frees tensor memory at once,
+//     then writes four 32 x 32 blocks through its own 64-byte-swizzled
+//     shared-memory buffer with TMA stores, so the global writes are
+//     whole-line and asynchronous while the next tile's MMAs run.
 // M and N tails come from the TMA out-of-bounds zero fill on loads and the
 // TMA clipping of stores; a K tail (K % 64 == 32) reads zero codes past K.
 #include <algorithm>
@@ -56,7 +57,7 @@ constexpr int kRowsPerCta = 128;        // rows of A (and of B) held by each CTA
 constexpr int kBN = 256;                // columns of C per tile
 constexpr int kBK = 256;                // K elements per stage
 constexpr int kBKBytes = kBK / 2;       // 128 bytes = one swizzle row
-constexpr int kStages = 5;
+constexpr int kStages = 6;
 constexpr int kAStage = kRowsPerCta * kBKBytes;  // 16 KiB
 constexpr int kBStage = kRowsPerCta * kBKBytes;  // 16 KiB
 constexpr int kSfaStage = 2 * 512;               // own 128-row tile x 2 K tiles
@@ -75,8 +76,13 @@ constexpr uint32_t kSfStageCols = kSfaCols + 16;  // + 2 K tiles x 2 row tiles x
 static_assert(kSfCol0 + kStages * kSfStageCols <= kTmemCols, "tensor memory budget");
 
 constexpr int kRingBytes = kStages * static_cast<int>(kStageBytes);
-constexpr int kOutStageBytes = 32 * 64 * 2;  // per epilogue warp: 32 rows x 64 bf16 columns
-constexpr int kSmemBytes = kRingBytes + kEpiWarps * kOutStageBytes + 512 + 1024;
+constexpr int kOutStageBytes = 32 * 32 * 2;  // per epilogue warp: 32 rows x 32 bf16 columns
+constexpr int kBarrierBytes = (3 * kStages + 2) * 8 + 16;
+// The dynamic shared-memory window starts 1024-byte aligned in practice; the
+// spare bytes below cover a smaller alignment and the kernel checks it.
+constexpr int kSmemBytes = 232448;
+static_assert(kRingBytes + kEpiWarps * kOutStageBytes + kBarrierBytes <= kSmemBytes, "shared memory");
+constexpr uint32_t kSmemSlack = kSmemBytes - (kRingBytes + kEpiWarps * kOutStageBytes + kBarrierBytes);
 
 // Instruction descriptor, kind::mxf4: A and B E2M1 (format 1), both K-major,
 // fp32 accumulator, N >> 3 at bit 17, UE8M0 scales (bit 23), M >> 4 at bit
@@ -120,7 +126,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 1024-byte alignment for the 128-byte-swizzled operand tiles (same offset
   // in both CTAs: identical kernels, identical static layout).
   const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+  if (pad > kSmemSlack) {  // cannot place the ring: report and leave (uniform over the grid)
+    if (threadIdx.x == 0) atomicExch(&g_device_status, 5 /* MXFP4_ERR_CUDA */);
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kAStage;
   uint8_t* sSfa = sB + kStages * kBStage;
@@ -293,40 +304,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_coords(t, p.num_mt, p.num_nt, mt, nt);
       if (!mbar_wait(acc_full, acc_phase, abort_flag, &g_device_status)) break;
       tc_fence_after();
-      // Two rounds of 64 columns: load, convert to bf16 pairs, stage, store;
-      // tensor memory is released as soon as the last columns are in registers.
+      // Read all 128 columns (4 x 32) as bf16 pairs, then release the accumulator.
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + h * 128;
       const int32_t row0 = mt * kBM + static_cast<int32_t>(rank) * kRowsPerCta + q * 32;
       const int32_t col0 = nt * kBN + h * 128;
+      uint32_t pk[64];
 #pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t r0[32], r1[32];
-        tmem_ld_32x32b_x32(taddr + c2 * 64, r0);
-        tmem_ld_32x32b_x32(taddr + c2 * 64 + 32, r1);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, r);
         tmem_ld_wait();
-        if (c2 == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(acc_empty_leader);  // accumulator free for the next tile
-        }
-        uint32_t pk[32];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          pk[j] = pack_bf16x2(r0[2 * j], r0[2 * j + 1]);
-          pk[16 + j] = pack_bf16x2(r1[2 * j], r1[2 * j + 1]);
-        }
-        // the previous store out of this buffer must have finished reading it
-        if (lane == 0) bulk_wait_group_read0();
+        for (int j = 0; j < 16; ++j) pk[c * 16 + j] = pack_bf16x2(r[2 * j], r[2 * j + 1]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_leader);  // accumulator free for the next tile
+      // Four 32 x 32 blocks: row `lane` is 64 bytes = four 16-byte chunks, chunk j
+      // stored at j ^ ((row / 2) % 4) (the 64-byte swizzle), conflict-free.
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (lane == 0) bulk_wait_group_read0();  // the previous block has left the buffer
         __syncwarp();
-        // row `lane` of the block: eight 16-byte chunks, chunk j at j ^ (row % 8)
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          sts128(out_buf + lane * 128 + ((j ^ (lane & 7)) * 16), pk[4 * j], pk[4 * j + 1],
-                 pk[4 * j + 2], pk[4 * j + 3]);
+        for (int j = 0; j < 4; ++j)
+          sts128(out_buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16), pk[c * 16 + 4 * j],
+                 pk[c * 16 + 4 * j + 1], pk[c * 16 + 4 * j + 2], pk[c * 16 + 4 * j + 3]);
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tmC, sOut + (warp - kFirstEpiWarp) * kOutStageBytes, col0 + c2 * 64, row0);
+          tma_store_2d(&tmC, sOut + (warp - kFirstEpiWarp) * kOutStageBytes, col0 + c * 32, row0);
           bulk_commit_group();
         }
       }
@@ -366,17 +373,17 @@ bool make_byte_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t 
   return r == CUDA_SUCCESS;
 }
 
-// Output map: bf16 [M, N] with row pitch ldc elements, boxes of 32 rows x 64
-// columns (128 bytes, 128-byte swizzle); stores clip at M and N.
+// Output map: bf16 [M, N] with row pitch ldc elements, boxes of 32 rows x 32
+// columns (64 bytes, 64-byte swizzle); stores clip at M and N.
 bool make_bf16_out_map(CUtensorMap* map, uint16_t* base, int64_t M, int64_t N, int64_t ldc) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * 2};
-  cuuint32_t box[2] = {64, 32};
+  cuuint32_t box[2] = {32, 32};
   cuuint32_t estrides[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estrides,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
