@@ -16,17 +16,16 @@
 //     128 x 128 tiles of x; each tile arrives in shared memory by one TMA
 //     load (zero fill past the edges) into a double buffer, so the next
 //     tile's load overlaps this tile's arithmetic and stores;
-//   * row pass: 16-byte coalesced loads, 4 lanes per 32-element block (8
-//     elements each); block amax as a packed 16-bit unsigned max of the bf16
-//     magnitudes plus two xor-shuffles (NaN/Inf sort above every finite
-//     value); the power-of-two scaling as an exact bf16x2 multiply; packing
-//     by cvt.rn.satfinite.e2m1x2.f32 (which keeps the sign of values that
-//     round to zero); the row-wise Hadamard as three in-register butterfly
-//     stages plus two shuffle stages;
+//   * row pass: from the shared-memory tile, 2 lanes per 32-element block
+//     (16 elements each); block amax as a packed, NaN-propagating bf16
+//     magnitude max plus one xor-shuffle; the power-of-two scaling as an
+//     exact bf16x2 multiply; packing by cvt.rn.satfinite.e2m1x2.f32 (which
+//     keeps the sign of values that round to zero); the row-wise Hadamard as
+//     four in-register butterfly stages plus one shuffle stage;
 //   * column pass: from the same shared-memory tile (untransformed); each
 //     thread takes a column pair x 32 rows (conflict-free 4-byte reads) and
 //     treats the two columns as the two halves of packed words -- one packed
-//     max gives both amaxes, one bf16x2 multiply scales both, and the column
+//     max per row gives both amaxes, one bf16x2 multiply scales both, and the column
 //     Hadamard runs both columns through one f32x2 butterfly network; 16
 //     bytes of codes are stored per column;
 //   * a 128 x 128 tile owns exactly one 512-byte scale tile of each output
@@ -66,20 +65,19 @@ __device__ __forceinline__ uint32_t cvt8_e2m1(float v0, float v1, float v2, floa
 
 __device__ __forceinline__ uint32_t abs_bits(float f) { return __float_as_uint(f) & 0x7FFFFFFFu; }
 
-// Two 16-bit unsigned maxima at once.  On bf16 magnitudes (sign bit cleared)
-// unsigned order is numeric order, with Inf and every NaN above all finite
-// values, so the maximum also flags non-finite blocks.
-__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
 // max(m, |x|) with NaN propagation (an Inf or NaN anywhere makes the block
 // non-finite).
 __device__ __forceinline__ float max_nan_abs(float m, float x) {
   float r;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(x)));
+  return r;
+}
+
+// Elementwise max(|a|, |b|) of bf16 pairs, NaN-propagating (sign bits of
+// the result are the XOR of the inputs' and must be masked off).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 
@@ -158,32 +156,6 @@ __device__ __forceinline__ uint32_t quantize8_bf16(uint32_t w0, uint32_t w1, uin
 // fp32 value nearest to 1/sqrt(32).
 constexpr float kInvSqrt32 = 0x1.6a09e6p-3f;  // bit pattern 0x3E3504F3
 
-// Butterfly stages h = 1, 2, 4 of the 32-point transform on this thread's 8
-// consecutive elements: pair (j, j+h), j & h == 0, becomes (a + b, a - b).
-__device__ __forceinline__ void fwht_local8(float* y) {
-#pragma unroll
-  for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j & h) continue;
-      const float a = y[j], b = y[j + h];
-      y[j] = __fadd_rn(a, b);
-      y[j + h] = __fsub_rn(a, b);
-    }
-  }
-}
-
-// Stage across lanes: this lane's element j pairs with element j of lane
-// (lane ^ lane_mask).  The lane holding the lower index keeps a + b, the
-// other keeps a - b with a the lower lane's value.
-__device__ __forceinline__ void fwht_cross(float* y, int lane_mask, bool upper) {
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float p = __shfl_xor_sync(kFullMask, y[j], lane_mask);
-    y[j] = upper ? __fsub_rn(p, y[j]) : __fadd_rn(y[j], p);
-  }
-}
-
 __device__ __forceinline__ int sf_in_tile(int r, int b) { return (r & 31) * 16 + (r >> 5) * 4 + b; }
 
 constexpr int kTileBytes = kTile * kTile * 2;  // one 128 x 128 bf16 tile
@@ -238,55 +210,71 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int64_t r0 = static_cast<int64_t>(t / col_tiles) * kTile;
   const int tile_x = t % col_tiles, tile_y = t / col_tiles;
 
-  // Iteration i covers tile rows 16i .. 16i+15: warp w takes rows 16i+2w and
-  // 16i+2w+1, 16 lanes x 8 elements per row.
-  const int c8 = (lane & 15) * 8;
-  const bool col_ok = c0 + c8 < cols;  // cols is a multiple of 32
-
   // ---------------------------------------------------------------- row pass
+  // Iteration it covers tile rows 32 it .. 32 it + 31: warp w takes rows
+  // 32 it + 4 w .. + 3; two lanes per 32-element block, 16 elements each.
   if constexpr (kRow) {
     const bool had = (args.flags & kFlagHadamardRow) != 0;
-    const int q = lane & 3;  // which 8 of the block's 32 elements
-    const int kb = (lane & 15) >> 2;
+    const int kb = (lane >> 1) & 3;  // block of the row (tile-local)
+    const int hf = lane & 1;         // which 16 of the block's 32 elements
+    const int e0 = kb * 32 + hf * 16;
+    const bool col_ok = c0 + kb * 32 < cols;  // cols is a multiple of 32
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int row = i * 16 + warp * 2 + (lane >> 4);
-      const uint4 vi = *reinterpret_cast<const uint4*>(xs + row * kTile + c8);
-      uint32_t codes;
+    for (int it = 0; it < 4; ++it) {
+      const int row = it * 32 + warp * 4 + (lane >> 3);
+      const uint4 va = *reinterpret_cast<const uint4*>(xs + row * kTile + e0);
+      const uint4 vb = *reinterpret_cast<const uint4*>(xs + row * kTile + e0 + 8);
+      uint2 codes;
       BlockScale s;
       if (!had) {
-        // block amax on the packed bf16 magnitudes, then across the 4 lanes
-        uint32_t m = max_u16x2(max_u16x2(vi.x & 0x7FFF7FFFu, vi.y & 0x7FFF7FFFu),
-                               max_u16x2(vi.z & 0x7FFF7FFFu, vi.w & 0x7FFF7FFFu));
-        m = max(m & 0xFFFFu, m >> 16);
-        m = max(m, __shfl_xor_sync(kFullMask, m, 1));
-        m = max(m, __shfl_xor_sync(kFullMask, m, 2));
-        s = block_scale(m << 16);
-        codes = s.nonfinite ? 0u
-                            : quantize8_bf16(vi.x, vi.y, vi.z, vi.w, s.mult_bf16 * 0x00010001u);
+        uint32_t m = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(va.x, va.y), absmax_bf16x2(va.z, va.w)),
+                                   absmax_bf16x2(absmax_bf16x2(vb.x, vb.y), absmax_bf16x2(vb.z, vb.w)));
+        m = absmax_bf16x2(m, __shfl_xor_sync(kFullMask, m, 1));
+        m = absmax_bf16x2(m, __byte_perm(m, 0, 0x1032));  // both halves hold the block max
+        s = block_scale((m & 0x7FFFu) << 16);
+        const uint32_t mult2 = s.mult_bf16 * 0x00010001u;
+        codes.x = quantize8_bf16(va.x, va.y, va.z, va.w, mult2);
+        codes.y = quantize8_bf16(vb.x, vb.y, vb.z, vb.w, mult2);
+        if (s.nonfinite) codes = make_uint2(0u, 0u);
       } else {
-        float y[8] = {bf16lo(vi.x), bf16hi(vi.x), bf16lo(vi.y), bf16hi(vi.y),
-                      bf16lo(vi.z), bf16hi(vi.z), bf16lo(vi.w), bf16hi(vi.w)};
-        fwht_local8(y);
-        fwht_cross(y, 1, (q & 1) != 0);
-        fwht_cross(y, 2, (q & 2) != 0);
+        // 32-point transform: stages h = 1, 2, 4, 8 inside the lane's 16
+        // elements, h = 16 across the lane pair.
+        float y[16] = {bf16lo(va.x), bf16hi(va.x), bf16lo(va.y), bf16hi(va.y),
+                       bf16lo(va.z), bf16hi(va.z), bf16lo(va.w), bf16hi(va.w),
+                       bf16lo(vb.x), bf16hi(vb.x), bf16lo(vb.y), bf16hi(vb.y),
+                       bf16lo(vb.z), bf16hi(vb.z), bf16lo(vb.w), bf16hi(vb.w)};
+#pragma unroll
+        for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (j & h) continue;
+            const float a = y[j], b = y[j + h];
+            y[j] = __fadd_rn(a, b);
+            y[j + h] = __fsub_rn(a, b);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float q = __shfl_xor_sync(kFullMask, y[j], 1);
+          y[j] = hf ? __fsub_rn(q, y[j]) : __fadd_rn(y[j], q);
+        }
         uint32_t amax = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 16; ++j) {
           y[j] = __fmul_rn(y[j], kInvSqrt32);
           amax = max(amax, abs_bits(y[j]));
         }
         amax = max(amax, __shfl_xor_sync(kFullMask, amax, 1));
-        amax = max(amax, __shfl_xor_sync(kFullMask, amax, 2));
         s = block_scale(amax);
-        codes = quantize8(y, s);
+        codes.x = quantize8(y, s);
+        codes.y = quantize8(y + 8, s);
       }
       const int64_t grow = r0 + row;
       if (col_ok && grow < rows)
-        *reinterpret_cast<uint32_t*>(args.q_row + grow * (cols / 2) + (c0 + c8) / 2) = codes;
-      if (q == 0) {
+        *reinterpret_cast<uint2*>(args.q_row + grow * (cols / 2) + (c0 + e0) / 2) = codes;
+      if (hf == 0) {
         if (linear) {
-          if (col_ok && grow < rows) args.sf_row[grow * (cols / 32) + (c0 + c8) / 32] = (uint8_t)s.byte;
+          if (col_ok && grow < rows) args.sf_row[grow * (cols / 32) + (c0 / 32) + kb] = (uint8_t)s.byte;
         } else {
           sf_row_tile[sf_in_tile(row, kb)] = (uint8_t)s.byte;
         }
@@ -306,9 +294,10 @@ __global__ void __launch_bounds__(kThreads, 3)
     BlockScale sa, sb;
     uint4 ca, cb;  // codes of column 2p and 2p+1
     if (!had) {
-      uint32_t m = 0;
+      uint32_t m = w[0];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) m = max_u16x2(m, w[i] & 0x7FFF7FFFu);
+      for (int i = 1; i < 32; ++i) m = absmax_bf16x2(m, w[i]);
+      m &= 0x7FFF7FFFu;
       sa = block_scale(m << 16);
       sb = block_scale(m & 0xFFFF0000u);
       const uint32_t mult2 = sa.mult_bf16 | (sb.mult_bf16 << 16);
