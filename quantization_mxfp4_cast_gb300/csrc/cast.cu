@@ -13,15 +13,16 @@
 // direction; the arithmetic is kept to a few instructions per element so the
 // ALU pipes stay below the memory rate):
 //   * persistent CTAs (as many as fit on the GPU), 256 threads each, walking
-//     128 x 128 tiles of x; each tile arrives in shared memory by one TMA
-//     load (zero fill past the edges) into a double buffer, so the next
-//     tile's load overlaps this tile's arithmetic and stores;
-//   * row pass: from the shared-memory tile, 2 lanes per 32-element block
-//     (16 elements each); block amax as a packed, NaN-propagating bf16
-//     magnitude max plus one xor-shuffle; the power-of-two scaling as an
-//     exact bf16x2 multiply; packing by cvt.rn.satfinite.e2m1x2.f32 (which
-//     keeps the sign of values that round to zero); the row-wise Hadamard as
-//     four in-register butterfly stages plus one shuffle stage;
+//     128 x 128 tiles of x; each tile arrives in shared memory by two TMA
+//     loads (64-column halves, 128-byte swizzle, zero fill past the edges)
+//     into a double buffer, so the next tile's load overlaps this tile's
+//     arithmetic and stores;
+//   * row pass: from the shared-memory tile, one lane per 32-element block
+//     (four 16-byte reads, conflict-free because of the swizzle); block amax
+//     as a tree of packed, NaN-propagating bf16 magnitude maxima; the
+//     power-of-two scaling as an exact bf16x2 multiply; packing by
+//     cvt.rn.satfinite.e2m1x2.f32 (which keeps the sign of values that round
+//     to zero); the row-wise Hadamard in registers;
 //   * column pass: from the same shared-memory tile (untransformed); each
 //     thread takes a column pair x 32 rows (conflict-free 4-byte reads) and
 //     treats the two columns as the two halves of packed words -- one packed
@@ -29,8 +30,9 @@
 //     Hadamard runs both columns through one f32x2 butterfly network; 16
 //     bytes of codes are stored per column;
 //   * a 128 x 128 tile owns exactly one 512-byte scale tile of each output
-//     (128 rows x 4 blocks), assembled in shared memory and written with one
-//     coalesced store, padding included.
+//     (128 rows x 4 blocks), assembled in shared memory (double-buffered, so
+//     one barrier per tile suffices) and written with one coalesced store,
+//     padding included.
 #include <algorithm>
 #include <atomic>
 
@@ -42,7 +44,6 @@ namespace {
 
 constexpr int kTile = 128;
 constexpr int kThreads = 256;
-constexpr uint32_t kFullMask = 0xFFFFFFFFu;
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -61,16 +62,6 @@ __device__ __forceinline__ uint32_t cvt8_e2m1(float v0, float v1, float v2, floa
       : "=r"(out)
       : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
   return out;
-}
-
-__device__ __forceinline__ uint32_t abs_bits(float f) { return __float_as_uint(f) & 0x7FFFFFFFu; }
-
-// max(m, |x|) with NaN propagation (an Inf or NaN anywhere makes the block
-// non-finite).
-__device__ __forceinline__ float max_nan_abs(float m, float x) {
-  float r;
-  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(x)));
-  return r;
 }
 
 // Elementwise max(|a|, |b|) of bf16 pairs, NaN-propagating (sign bits of
@@ -141,16 +132,31 @@ __device__ __forceinline__ uint32_t quantize8(const float* y, const BlockScale& 
                    __fmul_rn(y[6], m), __fmul_rn(y[7], m));
 }
 
+// fp32 value of the bf16 element in the low (kHi = false) or high half of w,
+// times s (a bf16 bit pattern), by the mixed-precision fma with -0 added:
+// for a power-of-two s the product is exact in fp32 down to 2^-126 (anything
+// smaller has |v| < 1/4 and gives a signed zero code either way), and adding
+// -0 keeps the sign of a zero product.  With s = 1 this is the plain widening.
+template <bool kHi>
+__device__ __forceinline__ float bf16_times(uint32_t w, uint16_t s) {
+  float r;
+  if constexpr (kHi)
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tfma.rn.f32.bf16 %0, h, %2, 0f80000000;\n\t}"
+        : "=f"(r) : "r"(w), "h"(s));
+  else
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tfma.rn.f32.bf16 %0, l, %2, 0f80000000;\n\t}"
+        : "=f"(r) : "r"(w), "h"(s));
+  return r;
+}
+constexpr uint16_t kBf16One = 0x3F80;
+
 // Codes of the 8 bf16 elements in 4 packed words (element 2i in the low half
-// of word i), scaled in bf16: the product of a bf16 and a power of two is
-// exact down to 2^-126, and anything smaller rounds to a signed zero code
-// either way.
+// of word i), scaled by the power of two s (bf16 bit pattern).
 __device__ __forceinline__ uint32_t quantize8_bf16(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
-                                                   uint32_t mult2) {
-  const uint32_t p0 = mul_bf16x2(w0, mult2), p1 = mul_bf16x2(w1, mult2);
-  const uint32_t p2 = mul_bf16x2(w2, mult2), p3 = mul_bf16x2(w3, mult2);
-  return cvt8_e2m1(bf16lo(p0), bf16hi(p0), bf16lo(p1), bf16hi(p1), bf16lo(p2), bf16hi(p2),
-                   bf16lo(p3), bf16hi(p3));
+                                                   uint16_t s) {
+  return cvt8_e2m1(bf16_times<false>(w0, s), bf16_times<true>(w0, s), bf16_times<false>(w1, s),
+                   bf16_times<true>(w1, s), bf16_times<false>(w2, s), bf16_times<true>(w2, s),
+                   bf16_times<false>(w3, s), bf16_times<true>(w3, s));
 }
 
 // fp32 value nearest to 1/sqrt(32).
@@ -158,19 +164,67 @@ constexpr float kInvSqrt32 = 0x1.6a09e6p-3f;  // bit pattern 0x3E3504F3
 
 __device__ __forceinline__ int sf_in_tile(int r, int b) { return (r & 31) * 16 + (r >> 5) * 4 + b; }
 
-constexpr int kTileBytes = kTile * kTile * 2;  // one 128 x 128 bf16 tile
-constexpr int kCastSmemBytes = 2 * kTileBytes + 2 * 512 + 64 + 128;
+// max(|a|, |b|, |c|) with NaN propagation (three-input form).
+__device__ __forceinline__ float max3_nan_abs(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)), "f"(fabsf(c)));
+  return r;
+}
+
+// Packed bf16 magnitude max of 2^n words as a balanced tree (independent
+// operations instead of one serial chain).  Sign bits of the result are
+// meaningless.
+template <int kN>
+__device__ __forceinline__ uint32_t tree_absmax_bf16x2(const uint32_t* w) {
+  uint32_t m[kN / 2];
+#pragma unroll
+  for (int i = 0; i < kN / 2; ++i) m[i] = absmax_bf16x2(w[2 * i], w[2 * i + 1]);
+#pragma unroll
+  for (int n = kN / 4; n >= 1; n >>= 1) {
+#pragma unroll
+    for (int i = 0; i < n; ++i) m[i] = absmax_bf16x2(m[2 * i], m[2 * i + 1]);
+  }
+  return m[0];
+}
+
+// NaN-propagating max |v| of 32 fp32 values read as v(i), i = 0..31, in four
+// independent chains of three-input maxima.
+template <typename F>
+__device__ __forceinline__ float amax32(F v) {
+  float c[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int b = 8 * k;
+    float m = max3_nan_abs(v(b), v(b + 1), v(b + 2));
+    m = max3_nan_abs(m, v(b + 3), v(b + 4));
+    m = max3_nan_abs(m, v(b + 5), v(b + 6));
+    c[k] = max3_nan_abs(m, v(b + 7), 0.f);
+  }
+  return max3_nan_abs(c[0], c[1], max3_nan_abs(c[2], c[3], 0.f));
+}
+
+// A 128 x 128 bf16 tile in shared memory is two 128-row halves of 64 columns
+// (128 bytes per row), each written by one TMA load with the 128-byte
+// swizzle: the 16-byte chunk k of row r sits at chunk position k ^ (r % 8).
+// Both passes below read it without bank conflicts: eight lanes reading the
+// same chunk of eight consecutive rows, or 32 lanes reading 4-byte words of
+// one row, always land on distinct banks.
+constexpr int kHalfBytes = kTile * 128;
+constexpr int kTileBytes = 2 * kHalfBytes;
+constexpr int kSfTileBytes = 512;
+constexpr int kCastSmemBytes = 2 * kTileBytes + 4 * kSfTileBytes + 64 + 1024;
 
 template <bool kRow, bool kCol>
 __global__ void __launch_bounds__(kThreads, 3)
     cast_kernel(const __grid_constant__ CUtensorMap tmX, const CastArgs args, int col_tiles,
                 int num_tiles, int* status) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
-  uint16_t* bufs = reinterpret_cast<uint16_t*>(smem);  // two [128][128] bf16 tiles
-  uint8_t* sf_row_tile = smem + 2 * kTileBytes;
-  uint8_t* sf_col_tile = sf_row_tile + 512;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sf_col_tile + 512);
+  // 1024-byte alignment: the swizzle pattern follows address bits 7..9.
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* bufs = smem;                               // two tiles
+  uint8_t* sf_row_tiles = smem + 2 * kTileBytes;      // two 512-byte scale tiles (row output)
+  uint8_t* sf_col_tiles = sf_row_tiles + 2 * kSfTileBytes;  // two (column output)
+  uint64_t* full = reinterpret_cast<uint64_t*>(sf_col_tiles + 2 * kSfTileBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
 
   const int tid = threadIdx.x;
@@ -187,11 +241,14 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
   __syncthreads();
   // Tile t covers rows 128 * (t / col_tiles), columns 128 * (t % col_tiles).
-  // The TMA zero-fills whatever lies past the tensor's edge.
+  // The TMA zero-fills whatever lies past the tensor's edge (including a
+  // half that starts beyond the last column).
   auto issue = [&](int t, int b) {
+    const int x = (t % col_tiles) * kTile, y = (t / col_tiles) * kTile;
+    uint8_t* dst = bufs + b * kTileBytes;
     mbar_arrive_expect_tx(&full[b], kTileBytes);
-    tma_load_2d(bufs + b * kTile * kTile, &tmX, &full[b], (t % col_tiles) * kTile,
-                (t / col_tiles) * kTile);
+    tma_load_2d(dst, &tmX, &full[b], x, y);
+    tma_load_2d(dst + kHalfBytes, &tmX, &full[b], x + kTile / 2, y);
   };
   if (tid == 0) {
     tma_prefetch_desc(&tmX);
@@ -201,83 +258,87 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
   }
 
+  // Tile coordinates advance by the grid size each step.
+  int tile_x = static_cast<int>(blockIdx.x) % col_tiles;
+  int tile_y = static_cast<int>(blockIdx.x) / col_tiles;
+  const int step_x = static_cast<int>(gridDim.x) % col_tiles;
+  const int step_y = static_cast<int>(gridDim.x) / col_tiles;
+
   int it = 0;
   for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
   const int b = it & 1;
   if (!mbar_wait(&full[b], (it >> 1) & 1, abort_flag, status)) break;
-  const uint16_t* xs = bufs + b * kTile * kTile;  // xs[row * kTile + col]
-  const int64_t c0 = static_cast<int64_t>(t % col_tiles) * kTile;
-  const int64_t r0 = static_cast<int64_t>(t / col_tiles) * kTile;
-  const int tile_x = t % col_tiles, tile_y = t / col_tiles;
+  const uint8_t* tile = bufs + b * kTileBytes;
+  const int64_t c0 = static_cast<int64_t>(tile_x) * kTile;
+  const int64_t r0 = static_cast<int64_t>(tile_y) * kTile;
+  uint8_t* sf_row_tile = sf_row_tiles + b * kSfTileBytes;
+  uint8_t* sf_col_tile = sf_col_tiles + b * kSfTileBytes;
 
   // ---------------------------------------------------------------- row pass
-  // Iteration it covers tile rows 32 it .. 32 it + 31: warp w takes rows
-  // 32 it + 4 w .. + 3; two lanes per 32-element block, 16 elements each.
+  // One lane per 32-element block: warp w, lane l take tile row
+  // 8 w + (l % 8) (+ 64 in the second iteration), block l / 8 of that row.
   if constexpr (kRow) {
     const bool had = (args.flags & kFlagHadamardRow) != 0;
-    const int kb = (lane >> 1) & 3;  // block of the row (tile-local)
-    const int hf = lane & 1;         // which 16 of the block's 32 elements
-    const int e0 = kb * 32 + hf * 16;
-    const bool col_ok = c0 + kb * 32 < cols;  // cols is a multiple of 32
+    const int kb = lane >> 3;
+    const int xk = ((kb & 1) * 4) ^ (lane & 7);  // chunk 4 (kb % 2) + j sits at xk ^ j
+    const bool col_ok = c0 + kb * 32 < cols;      // cols is a multiple of 32
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int row = it * 32 + warp * 4 + (lane >> 3);
-      const uint4 va = *reinterpret_cast<const uint4*>(xs + row * kTile + e0);
-      const uint4 vb = *reinterpret_cast<const uint4*>(xs + row * kTile + e0 + 8);
-      uint2 codes;
+    for (int ri = 0; ri < 2; ++ri) {
+      const int row = warp * 8 + (lane & 7) + ri * 64;
+      const uint8_t* rowp = tile + (kb >> 1) * kHalfBytes + row * 128;
+      uint32_t v[16];  // elements 2i (low half), 2i + 1 of the block
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 q = *reinterpret_cast<const uint4*>(rowp + ((xk ^ j) << 4));
+        v[4 * j] = q.x;
+        v[4 * j + 1] = q.y;
+        v[4 * j + 2] = q.z;
+        v[4 * j + 3] = q.w;
+      }
+      uint4 codes;
       BlockScale s;
       if (!had) {
-        uint32_t m = absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(va.x, va.y), absmax_bf16x2(va.z, va.w)),
-                                   absmax_bf16x2(absmax_bf16x2(vb.x, vb.y), absmax_bf16x2(vb.z, vb.w)));
-        m = absmax_bf16x2(m, __shfl_xor_sync(kFullMask, m, 1));
+        uint32_t m = tree_absmax_bf16x2<16>(v);
         m = absmax_bf16x2(m, __byte_perm(m, 0, 0x1032));  // both halves hold the block max
         s = block_scale((m & 0x7FFFu) << 16);
-        const uint32_t mult2 = s.mult_bf16 * 0x00010001u;
-        codes.x = quantize8_bf16(va.x, va.y, va.z, va.w, mult2);
-        codes.y = quantize8_bf16(vb.x, vb.y, vb.z, vb.w, mult2);
-        if (s.nonfinite) codes = make_uint2(0u, 0u);
+        const uint16_t mb = static_cast<uint16_t>(s.mult_bf16);
+        codes.x = quantize8_bf16(v[0], v[1], v[2], v[3], mb);
+        codes.y = quantize8_bf16(v[4], v[5], v[6], v[7], mb);
+        codes.z = quantize8_bf16(v[8], v[9], v[10], v[11], mb);
+        codes.w = quantize8_bf16(v[12], v[13], v[14], v[15], mb);
+        if (s.nonfinite) codes = make_uint4(0u, 0u, 0u, 0u);
       } else {
-        // 32-point transform: stages h = 1, 2, 4, 8 inside the lane's 16
-        // elements, h = 16 across the lane pair.
-        float y[16] = {bf16lo(va.x), bf16hi(va.x), bf16lo(va.y), bf16hi(va.y),
-                       bf16lo(va.z), bf16hi(va.z), bf16lo(va.w), bf16hi(va.w),
-                       bf16lo(vb.x), bf16hi(vb.x), bf16lo(vb.y), bf16hi(vb.y),
-                       bf16lo(vb.z), bf16hi(vb.z), bf16lo(vb.w), bf16hi(vb.w)};
+        float y[32];
 #pragma unroll
-        for (int h = 1; h < 16; h <<= 1) {
+        for (int i = 0; i < 16; ++i) {
+          y[2 * i] = bf16_times<false>(v[i], kBf16One);
+          y[2 * i + 1] = bf16_times<true>(v[i], kBf16One);
+        }
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+        for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
             if (j & h) continue;
-            const float a = y[j], b = y[j + h];
-            y[j] = __fadd_rn(a, b);
-            y[j + h] = __fsub_rn(a, b);
+            const float a = y[j], c = y[j + h];
+            y[j] = __fadd_rn(a, c);
+            y[j + h] = __fsub_rn(a, c);
           }
         }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float q = __shfl_xor_sync(kFullMask, y[j], 1);
-          y[j] = hf ? __fsub_rn(q, y[j]) : __fadd_rn(y[j], q);
-        }
-        uint32_t amax = 0;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          y[j] = __fmul_rn(y[j], kInvSqrt32);
-          amax = max(amax, abs_bits(y[j]));
-        }
-        amax = max(amax, __shfl_xor_sync(kFullMask, amax, 1));
-        s = block_scale(amax);
+        for (int j = 0; j < 32; ++j) y[j] = __fmul_rn(y[j], kInvSqrt32);
+        s = block_scale(__float_as_uint(amax32([&](int i) { return y[i]; })));
         codes.x = quantize8(y, s);
         codes.y = quantize8(y + 8, s);
+        codes.z = quantize8(y + 16, s);
+        codes.w = quantize8(y + 24, s);
       }
       const int64_t grow = r0 + row;
       if (col_ok && grow < rows)
-        *reinterpret_cast<uint2*>(args.q_row + grow * (cols / 2) + (c0 + e0) / 2) = codes;
-      if (hf == 0) {
-        if (linear) {
-          if (col_ok && grow < rows) args.sf_row[grow * (cols / 32) + (c0 / 32) + kb] = (uint8_t)s.byte;
-        } else {
-          sf_row_tile[sf_in_tile(row, kb)] = (uint8_t)s.byte;
-        }
+        *reinterpret_cast<uint4*>(args.q_row + grow * (cols / 2) + (c0 + kb * 32) / 2) = codes;
+      if (linear) {
+        if (col_ok && grow < rows) args.sf_row[grow * (cols / 32) + (c0 / 32) + kb] = (uint8_t)s.byte;
+      } else {
+        sf_row_tile[sf_in_tile(row, kb)] = (uint8_t)s.byte;
       }
     }
   }
@@ -287,31 +348,33 @@ __global__ void __launch_bounds__(kThreads, 3)
     const bool had = (args.flags & kFlagHadamardCol) != 0;
     const int p = tid & 63;   // column pair: tile columns 2p (low halves), 2p+1 (high halves)
     const int rb = tid >> 6;  // 32-row block of the tile
+    const uint8_t* colp = tile + (p >> 5) * kHalfBytes + rb * 32 * 128 + (p & 3) * 4;
+    const int ch = (p & 31) >> 2;  // 16-byte chunk of the pair within its row half
     uint32_t w[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = *reinterpret_cast<const uint32_t*>(xs + (rb * 32 + i) * kTile + 2 * p);
+    for (int i = 0; i < 32; ++i)
+      w[i] = *reinterpret_cast<const uint32_t*>(colp + i * 128 + ((ch ^ (i & 7)) << 4));
     const bool rows_ok = r0 + rb * 32 < rows;  // rows is a multiple of 32
     BlockScale sa, sb;
     uint4 ca, cb;  // codes of column 2p and 2p+1
     if (!had) {
-      uint32_t m = w[0];
-#pragma unroll
-      for (int i = 1; i < 32; ++i) m = absmax_bf16x2(m, w[i]);
-      m &= 0x7FFF7FFFu;
+      const uint32_t m = tree_absmax_bf16x2<32>(w) & 0x7FFF7FFFu;
       sa = block_scale(m << 16);
       sb = block_scale(m & 0xFFFF0000u);
-      const uint32_t mult2 = sa.mult_bf16 | (sb.mult_bf16 << 16);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) w[i] = mul_bf16x2(w[i], mult2);
+      const uint16_t ma = static_cast<uint16_t>(sa.mult_bf16), mb = static_cast<uint16_t>(sb.mult_bf16);
       uint32_t* pa = &ca.x;
       uint32_t* pb = &cb.x;
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         const uint32_t* u = w + 8 * g;
-        pa[g] = cvt8_e2m1(bf16lo(u[0]), bf16lo(u[1]), bf16lo(u[2]), bf16lo(u[3]), bf16lo(u[4]),
-                          bf16lo(u[5]), bf16lo(u[6]), bf16lo(u[7]));
-        pb[g] = cvt8_e2m1(bf16hi(u[0]), bf16hi(u[1]), bf16hi(u[2]), bf16hi(u[3]), bf16hi(u[4]),
-                          bf16hi(u[5]), bf16hi(u[6]), bf16hi(u[7]));
+        pa[g] = cvt8_e2m1(bf16_times<false>(u[0], ma), bf16_times<false>(u[1], ma),
+                          bf16_times<false>(u[2], ma), bf16_times<false>(u[3], ma),
+                          bf16_times<false>(u[4], ma), bf16_times<false>(u[5], ma),
+                          bf16_times<false>(u[6], ma), bf16_times<false>(u[7], ma));
+        pb[g] = cvt8_e2m1(bf16_times<true>(u[0], mb), bf16_times<true>(u[1], mb),
+                          bf16_times<true>(u[2], mb), bf16_times<true>(u[3], mb),
+                          bf16_times<true>(u[4], mb), bf16_times<true>(u[5], mb),
+                          bf16_times<true>(u[6], mb), bf16_times<true>(u[7], mb));
       }
       if (sa.nonfinite) ca = make_uint4(0u, 0u, 0u, 0u);
       if (sb.nonfinite) cb = make_uint4(0u, 0u, 0u, 0u);
@@ -319,25 +382,21 @@ __global__ void __launch_bounds__(kThreads, 3)
       // both columns through one 32-point butterfly network on fp32 pairs
       uint64_t y[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) y[i] = pk2(bf16lo(w[i]), bf16hi(w[i]));
+      for (int i = 0; i < 32; ++i) y[i] = pk2(bf16_times<false>(w[i], kBf16One), bf16_times<true>(w[i], kBf16One));
 #pragma unroll
       for (int h = 1; h < 32; h <<= 1) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           if (j & h) continue;
-          const uint64_t a = y[j], b = y[j + h];
-          y[j] = add2(a, b);
-          y[j + h] = sub2(a, b);
+          const uint64_t a = y[j], c = y[j + h];
+          y[j] = add2(a, c);
+          y[j + h] = sub2(a, c);
         }
       }
       // amax of the transformed block: rounding is monotonic, so the largest
       // |RN(h * c)| is RN(max |h| * c); the NaN-propagating max keeps NaN/Inf.
-      float ha = 0.f, hb = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        ha = max_nan_abs(ha, lo2(y[i]));
-        hb = max_nan_abs(hb, hi2(y[i]));
-      }
+      const float ha = amax32([&](int i) { return lo2(y[i]); });
+      const float hb = amax32([&](int i) { return hi2(y[i]); });
       sa = block_scale(__float_as_uint(__fmul_rn(ha, kInvSqrt32)));
       sb = block_scale(__float_as_uint(__fmul_rn(hb, kInvSqrt32)));
       // v = RN(h * c) * 2^-e.  For scale bytes 3..250 this equals
@@ -383,7 +442,12 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 
   // ---------------------------------------------------------------- scale tiles
-  __syncthreads();  // the tile buffer is consumed and both scale tiles are complete
+  // One barrier per tile: the tile buffer is consumed and both scale tiles
+  // are complete.  The scale tiles are double-buffered, so the next tile's
+  // passes write the other pair while warps 0 and 1 copy these out; the
+  // pair is reused only after the next tile's barrier, which those warps
+  // reach after their copies.
+  __syncthreads();
   if (tid == 0) {
     const int tn = t + 2 * static_cast<int>(gridDim.x);
     if (tn < num_tiles) {
@@ -393,23 +457,28 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
   if (!linear) {
     if constexpr (kRow) {
-      if (tid < 32) {
+      if (warp == 0) {
         const int64_t ktiles = (cols + kTile - 1) / kTile;
-        const int64_t tile = static_cast<int64_t>(tile_y) * ktiles + tile_x;
-        reinterpret_cast<uint4*>(args.sf_row + tile * 512)[tid] =
-            reinterpret_cast<const uint4*>(sf_row_tile)[tid];
+        const int64_t tile_idx = static_cast<int64_t>(tile_y) * ktiles + tile_x;
+        reinterpret_cast<uint4*>(args.sf_row + tile_idx * 512)[lane] =
+            reinterpret_cast<const uint4*>(sf_row_tile)[lane];
       }
     }
     if constexpr (kCol) {
-      if (tid >= 32 && tid < 64) {
+      if (warp == 1) {
         const int64_t ktiles = (rows + kTile - 1) / kTile;
-        const int64_t tile = static_cast<int64_t>(tile_x) * ktiles + tile_y;
-        reinterpret_cast<uint4*>(args.sf_col + tile * 512)[tid - 32] =
-            reinterpret_cast<const uint4*>(sf_col_tile)[tid - 32];
+        const int64_t tile_idx = static_cast<int64_t>(tile_x) * ktiles + tile_y;
+        reinterpret_cast<uint4*>(args.sf_col + tile_idx * 512)[lane] =
+            reinterpret_cast<const uint4*>(sf_col_tile)[lane];
       }
     }
   }
-  __syncthreads();  // scale tiles written out before the next tile refills them
+  tile_x += step_x;
+  tile_y += step_y;
+  if (tile_x >= col_tiles) {
+    tile_x -= col_tiles;
+    ++tile_y;
+  }
   }
 }
 
@@ -452,10 +521,10 @@ cudaError_t launch_cast(const CastArgs& args, cudaStream_t stream) {
   CUtensorMap tm;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(args.cols), static_cast<cuuint64_t>(args.rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(args.ldx) * 2};
-  cuuint32_t box[2] = {kTile, kTile};
+  cuuint32_t box[2] = {kTile / 2, kTile};  // 64 columns (128 bytes) x 128 rows
   cuuint32_t estrides[2] = {1, 1};
   if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(args.x), dims, strides, box,
-         estrides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+         estrides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   int dev = 0;

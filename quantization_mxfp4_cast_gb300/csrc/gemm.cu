@@ -29,6 +29,9 @@
 //     tcgen05.mma.kind::mxf4 per stage (K = 64, two UE8M0 scales per row each)
 //     update a 256 x 256 fp32 accumulator (128 lanes x 256 columns in each
 //     SM); tcgen05.commit multicasts the stage release to both CTAs.  The
+//     warp stays converged and one elected lane issues, with the operand
+//     descriptors precomputed (the issue rate of this one warp bounds the
+//     whole GEMM: ~55 cycles per MMA this way, ~93 from a lone lane).  The
 //     stagers of both CTAs report "stage ready" straight to the first CTA's
 //     barrier (their own data has landed by then), so no relay hop;
 //   * warps 6-13: epilogue -- each warp reads 32 lanes x 128 columns of the
@@ -218,41 +221,57 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (leader) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        uint32_t stage = 0, phase = 0, acc_phase = 0;
-        bool ok = true;
-        for (int t = pair; ok && t < num_tiles; t += num_pairs) {
-          if (!mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, &g_device_status)) break;
+      // The whole warp runs the loop (so the descriptors stay warp-uniform)
+      // and one elected lane issues each stage's MMAs and the commit.
+      // Measured: issuing from a lone lane of a diverged warp cost ~93 cycles
+      // per tcgen05.mma and left the tensor pipe idle half the time; from a
+      // converged warp with precomputed descriptors it is ~55 cycles.
+      uint32_t stage = 0, phase = 0, acc_phase = 0;
+      bool ok = true;
+      const uint64_t adesc0 = make_smem_desc(smem_u32(sA), 16, 1024, 2);
+      const uint64_t bdesc0 = make_smem_desc(smem_u32(sB), 16, 1024, 2);
+      // 64-deep k-steps of the last stage (K % 64 == 32 rounds up: zero codes).
+      const int last_nks =
+          static_cast<int>((args.K - static_cast<int64_t>(p.num_kt - 1) * kBK + 63) / 64);
+      for (int t = pair; ok && t < num_tiles; t += num_pairs) {
+        ok = mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, &g_device_status);
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+        tc_fence_after();
+        for (int kt = 0; kt < p.num_kt; ++kt) {
+          ok = mbar_wait(&sf_ready[stage], phase, abort_flag, &g_device_status);
+          if (!__all_sync(0xFFFFFFFFu, ok)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          for (int kt = 0; kt < p.num_kt; ++kt) {
-            if (!mbar_wait(&sf_ready[stage], phase, abort_flag, &g_device_status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t sf_col = tmem_base + kSfCol0 + stage * kSfStageCols;
-            const uint32_t a_addr = smem_u32(sA + stage * kAStage);
-            const uint32_t b_addr = smem_u32(sB + stage * kBStage);
+          // Descriptor start addresses are in 16-byte units: a stage is
+          // kAStage / 16 further, a 64-deep k-step 32 bytes (2 units).
+          const uint64_t a_d = adesc0 + ((stage * kAStage) >> 4);
+          const uint64_t b_d = bdesc0 + ((stage * kBStage) >> 4);
+          const uint32_t sf_col = tmem_base + kSfCol0 + stage * kSfStageCols;
+          const int nks = kt + 1 < p.num_kt ? 4 : last_nks;
+          if (elect_one_sync()) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-              if (static_cast<int64_t>(kt) * kBK + ks * 64 >= args.K) break;
-              const uint32_t g = ks >> 1, sf_id = (ks & 1) * 2;
-              const uint64_t adesc = make_smem_desc(a_addr + ks * 32, 16, 1024, 2);
-              const uint64_t bdesc = make_smem_desc(b_addr + ks * 32, 16, 1024, 2);
-              const uint32_t idesc = kIdescBase | (sf_id << 4) | (sf_id << 29);
-              tc_mma_pair_mxf4(tmem_base + kAccCol, adesc, bdesc, idesc, sf_col + g * 4,
-                               sf_col + kSfaCols + g * 8, (kt | ks) != 0);
+              if (ks < nks) {
+                const uint32_t sf_id = (ks & 1) * 2;
+                tc_mma_pair_mxf4(tmem_base + kAccCol, a_d + 2 * ks, b_d + 2 * ks,
+                                 kIdescBase | (sf_id << 4) | (sf_id << 29), sf_col + (ks >> 1) * 4,
+                                 sf_col + kSfaCols + (ks >> 1) * 8, (kt | ks) != 0);
+              }
             }
             tc_commit_pair(&empty[stage], 0x3);
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1u;
-            }
           }
-          if (!ok) break;
-          tc_commit_pair(acc_full, 0x3);
-          acc_phase ^= 1u;
+          __syncwarp();
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
+        if (!ok) break;
+        if (elect_one_sync()) tc_commit_pair(acc_full, 0x3);
+        __syncwarp();
+        acc_phase ^= 1u;
       }
     }
   } else if (warp < kFirstEpiWarp) {
