@@ -454,7 +454,7 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         nthreads = cpu_threads()
-        est, spent, desc = oracle_sample(1024, 128, 512, nthreads)
+        est, spent, desc = oracle_sample(4096, 256, 1024, nthreads)  # ~10 s of CPU work
         cpu = {"value": STEP_FLOPS / est / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
                "sample": desc + f" ({spent:.1f} s of CPU work)"}
 
