@@ -10,8 +10,10 @@ quotes):
   three MXFP4 GEMMs -- fwd Y = X W^T, dgrad dX = dY W, wgrad dW = dY^T X.
 `value` is the step's GEMM TFLOP/s (3 x 2MNK per step over the step time,
 casts included) with inputs resident in HBM; `e2e` repeats it through the same
-C-ABI calls with host buffers (pinned H2D of X, W, dY and D2H of Y, dX, dW
-inside the timed region).  `--impl reference` times the CPU oracle instead.
+C-ABI calls with host buffers (pinned H2D of X, W, dY and D2H of Y, dX, dW of
+every step inside the timed region, double-buffered so that one step's uploads
+and downloads overlap its neighbours' compute).  `--impl reference` times the
+CPU oracle instead.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 (for N > 1 launch one process per GPU with torch.distributed.run).
@@ -183,16 +185,63 @@ class Step:
             if events is not None:
                 events[i][1].record(stream)
 
-    def run_e2e(self, stream):
+    def e2e_buffers(self, dev):
+        """A second set of bf16 inputs and outputs on the device, and two sets of
+        pinned host outputs, for the double-buffered end-to-end pipeline."""
+        bf = lambda r, c: torch.empty(r, c, dtype=torch.bfloat16, device=dev)
+        self.e2e_in = [(self.x, self.w, self.dy), (bf(M, K), bf(N, K), bf(M, N))]
+        self.e2e_out = [(self.y, self.dx, self.dw), (bf(M, N), bf(M, K), bf(N, K))]
+        pin = lambda r, c: torch.empty(r, c, dtype=torch.bfloat16).pin_memory()
+        self.e2e_host_out = [self.out_host, {"y": pin(M, N), "dx": pin(M, K), "dw": pin(N, K)}]
+
+    def launches_on(self, xs, outs, stream):
+        m = self.m
+        x, w, dy = xs
+        y, dx, dw = outs
+        return [
+            lambda: m.mxfp4_cast_dual(x, hadamard_col=True, out=self.qx, stream=stream),
+            lambda: m.mxfp4_cast_dual(w, out=self.qw, stream=stream),
+            lambda: m.mxfp4_cast_dual(dy, hadamard_col=True, out=self.qdy, stream=stream),
+            lambda: m.gemm_fp4(self.qx[0], self.qx[1], self.qw[0], self.qw[1], M, N, K, c=y, stream=stream),
+            lambda: m.gemm_fp4(self.qdy[0], self.qdy[1], self.qw[2], self.qw[3], M, K, N, c=dx, stream=stream),
+            lambda: m.gemm_fp4(self.qdy[2], self.qdy[3], self.qx[2], self.qx[3], N, K, M, c=dw, stream=stream),
+        ]
+
+    def run_e2e_pipelined(self, n_steps, streams, ev):
+        """n_steps train steps from pinned host inputs to pinned host outputs.
+
+        Every step copies its inputs host->device (copy-in stream), runs the
+        casts and GEMMs (compute stream) and copies its three outputs
+        device->host (copy-out stream).  Inputs and outputs are double-buffered
+        so that step i+1's upload and step i-1's download overlap step i's
+        compute; events order every reuse of a buffer.  (Measured: one copy
+        stream per tensor and direction is slower than one per direction.)"""
+        s_in, s_comp, s_out = streams
         h = self.host
-        self.x.copy_(h["x"], non_blocking=True)
-        self.w.copy_(h["w"], non_blocking=True)
-        self.dy.copy_(h["dy"], non_blocking=True)
-        self.run(stream)
-        o = self.out_host
-        o["y"].copy_(self.y, non_blocking=True)
-        o["dx"].copy_(self.dx, non_blocking=True)
-        o["dw"].copy_(self.dw, non_blocking=True)
+        for i in range(n_steps):
+            b = i % 2
+            xs, outs, hout = self.e2e_in[b], self.e2e_out[b], self.e2e_host_out[b]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev["in_free"][b])      # step i-2's casts have read buffer b
+                for dst, src in zip(xs, (h["x"], h["w"], h["dy"])):
+                    dst.copy_(src, non_blocking=True)
+                ev["in_ready"][b].record(s_in)
+            s_comp.wait_event(ev["in_ready"][b])
+            if i >= 2:
+                s_comp.wait_event(ev["out_free"][b])       # step i-2's outputs have been downloaded
+            fs = self.launches_on(xs, outs, s_comp)
+            for f in fs[:3]:
+                f()
+            ev["in_free"][b].record(s_comp)
+            for f in fs[3:]:
+                f()
+            ev["out_ready"][b].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev["out_ready"][b])
+                for name, src in zip(("y", "dx", "dw"), outs):
+                    hout[name].copy_(src, non_blocking=True)
+                ev["out_free"][b].record(s_out)
 
     def h2d_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.host.values())
@@ -433,28 +482,33 @@ def main():
     e2e = None
     if not args.no_e2e:
         k_e2e = max(3, min(args.steps, 20))
-        with torch.cuda.stream(stream):
-            step.run_e2e(stream)
-        stream.synchronize()
+        step.e2e_buffers(dev)
+        streams = (torch.cuda.Stream(device=dev), stream, torch.cuda.Stream(device=dev))
+        ev = {k: [torch.cuda.Event(), torch.cuda.Event()] for k in ("in_ready", "in_free", "out_ready", "out_free")}
+        step.run_e2e_pipelined(2, streams, ev)  # warm-up
+        torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(k_e2e):
-                step.run_e2e(stream)
-            e1.record(stream)
-        stream.synchronize()
+        e0.record(stream)
+        for st in (streams[0], streams[2]):
+            st.wait_event(e0)
+        step.run_e2e_pipelined(k_e2e, streams, ev)
+        for st in (streams[0], streams[2]):
+            stream.wait_event(st.record_event())
+        e1.record(stream)
+        torch.cuda.synchronize()
         barrier(world)
         t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
         e2e = {"value": world * STEP_FLOPS * k_e2e / t_e2e / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": step.h2d_bytes(), "d2h_bytes_per_step": step.d2h_bytes(),
-               "steps": k_e2e, "ms_per_step": t_e2e / k_e2e * 1e3}
+               "steps": k_e2e, "ms_per_step": t_e2e / k_e2e * 1e3,
+               "pipeline": "double-buffered: upload of step i+1 and download of step i-1 overlap step i's compute"}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         nthreads = cpu_threads()
-        est, spent, desc = oracle_sample(4096, 256, 1024, nthreads)  # ~10 s of CPU work
+        est, spent, desc = oracle_sample(8192, 256, 1536, nthreads)  # ~10-15 s of CPU work
         cpu = {"value": STEP_FLOPS / est / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
                "sample": desc + f" ({spent:.1f} s of CPU work)"}
 
