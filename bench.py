@@ -9,7 +9,9 @@ quotes):
                        (column copy with the Hadamard);
   three MXFP4 GEMMs -- fwd Y = X W^T, dgrad dX = dY W, wgrad dW = dY^T X.
 `value` is the step's GEMM TFLOP/s (3 x 2MNK per step over the step time,
-casts included) with inputs resident in HBM; `e2e` repeats it through the same
+casts included) with inputs resident in HBM (the independent launches of a
+step run on three streams, so one kernel's tail overlaps the next one's start;
+--serial-step keeps them on one stream); `e2e` repeats it through the same
 C-ABI calls with host buffers (pinned H2D of X, W, dY and D2H of Y, dX, dW of
 every step inside the timed region, double-buffered so that one step's uploads
 and downloads overlap its neighbours' compute).  `--impl reference` times the
@@ -184,6 +186,41 @@ class Step:
             f()
             if events is not None:
                 events[i][1].record(stream)
+
+    def run_concurrent(self, stream, side):
+        """The same six launches with the independent ones on three streams:
+        the casts of X, W and dY side by side, then fwd (X, W), dgrad (dY, W)
+        and wgrad (dY, X) each as soon as its two casts are done.  Every
+        kernel fills the GPU; the overlap only fills the tail of one kernel
+        with the start of the next."""
+        s1, s2 = side
+        s1.wait_stream(stream)
+        s2.wait_stream(stream)
+        fs = [f for _, f in self.launches_streams((stream, s1, s2))]
+        fs[0]()                    # cast X  (stream)
+        fs[1]()                    # cast W  (s1)
+        fs[2]()                    # cast dY (s2)
+        e_x, e_w, e_dy = stream.record_event(), s1.record_event(), s2.record_event()
+        stream.wait_event(e_w)
+        fs[3]()                    # fwd   (stream): X, W
+        s1.wait_event(e_dy)
+        fs[4]()                    # dgrad (s1): dY, W
+        s2.wait_event(e_x)
+        fs[5]()                    # wgrad (s2): dY, X
+        stream.wait_stream(s1)
+        stream.wait_stream(s2)
+
+    def launches_streams(self, streams):
+        s0, s1, s2 = streams
+        m = self.m
+        return [
+            ("cast", lambda: m.mxfp4_cast_dual(self.x, hadamard_col=True, out=self.qx, stream=s0)),
+            ("cast", lambda: m.mxfp4_cast_dual(self.w, out=self.qw, stream=s1)),
+            ("cast", lambda: m.mxfp4_cast_dual(self.dy, hadamard_col=True, out=self.qdy, stream=s2)),
+            ("gemm", lambda: m.gemm_fp4(self.qx[0], self.qx[1], self.qw[0], self.qw[1], M, N, K, c=self.y, stream=s0)),
+            ("gemm", lambda: m.gemm_fp4(self.qdy[0], self.qdy[1], self.qw[2], self.qw[3], M, K, N, c=self.dx, stream=s1)),
+            ("gemm", lambda: m.gemm_fp4(self.qdy[2], self.qdy[3], self.qx[2], self.qx[3], N, K, M, c=self.dw, stream=s2)),
+        ]
 
     def e2e_buffers(self, dev):
         """A second set of bf16 inputs and outputs on the device, and two sets of
@@ -375,6 +412,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--serial-step", action="store_true",
+                    help="capture the six launches on one stream instead of three")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
         log("warmup raised to 3 (minimum)")
@@ -405,8 +444,12 @@ def main():
     # and replayed K times, so the host never starves the GPU between launches.
     n_launch = len(step.launches(stream))
     graph = torch.cuda.CUDAGraph()
+    side = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
     with torch.cuda.graph(graph, stream=stream):
-        step.run(stream)
+        if args.serial_step:
+            step.run(stream)
+        else:
+            step.run_concurrent(stream, side)
     with torch.cuda.stream(stream):
         for _ in range(3):
             graph.replay()
@@ -529,7 +572,9 @@ def main():
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": n_launch * args.steps,
-            "timing": {"timed_region": "CUDA-graph replay of the captured step, K times, CUDA events on the launch stream",
+            "timing": {"timed_region": ("CUDA-graph replay of the captured step, K times, CUDA events on the launch stream"
+                                 + ("" if args.serial_step else "; the step's independent launches on three "
+                                    "streams (three casts side by side, each GEMM after its two casts)")),
                        "per_kernel": f"{n_prof} eager steps enqueued behind a GPU sleep, an event pair per launch"},
             "clocks": clk.summary(),
         }
