@@ -287,6 +287,68 @@ class Step:
         return sum(t.numel() * t.element_size() for t in self.out_host.values())
 
 
+# ----------------------------------------------------------------------------- layer and FP8 legs
+def time_loop(fn, iters, warm, stream):
+    """Mean seconds per call of fn() on `stream` (CUDA events, after warm-up)."""
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            fn()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            fn()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / iters
+
+
+def layer_leg(step, stream, iters=10):
+    """The same train step through the layer API (MXFP4Linear: autograd
+    forward + backward) with the weight's casts served by the workspace, as
+    between two optimizer steps (micro-batches); gradients are dropped after
+    each micro-batch, so no accumulation kernel runs."""
+    from quantization_mxfp4_cast_gb300.layer import MXFP4Linear
+    with torch.cuda.stream(stream):
+        layer = MXFP4Linear(step.w.clone(), cache_name="down_proj")
+        x = step.x.detach().clone().requires_grad_(True)
+        dy = step.dy
+
+        def micro_batch():
+            y = layer(x)
+            y.backward(dy)
+            layer.weight.grad = None
+            x.grad = None
+
+        t = time_loop(micro_batch, iters, 2, stream)
+    return {"value": STEP_FLOPS / t / 1e12, "unit": "TFLOP/s", "ms_per_micro_batch": t * 1e3,
+            "weight_casts": layer.workspace.casts, "micro_batches": iters + 2,
+            "what": "MXFP4Linear fwd + bwd (casts of X and dY, three GEMMs) with W's casts cached "
+                    "in a WeightWorkspace across micro-batches"}
+
+
+def fp8_reference_leg(dev, stream, iters=20):
+    """cuBLASLt FP8 (e4m3, per-tensor scales, bf16 out) through torch._scaled_mm
+    on the step's three GEMM shapes, operands pre-quantized: context for the
+    FP4 GEMMs on the same GPU.  Not part of any timed value."""
+    try:
+        f8 = torch.float8_e4m3fn
+        out = {}
+        one = torch.ones((), device=dev, dtype=torch.float32)
+        for name, (mo, no, kc) in {"fwd": (M, N, K), "dgrad": (M, K, N), "wgrad": (N, K, M)}.items():
+            a = (torch.randn(mo, kc, device=dev) * 0.5).to(f8)
+            b = (torch.randn(no, kc, device=dev) * 0.5).to(f8)
+            fn = lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            t = time_loop(fn, iters, 3, stream)
+            out[name] = 2.0 * mo * no * kc / t / 1e12
+            del a, b
+        return {"unit": "TFLOP/s", "gemm_tflops": out,
+                "what": "torch._scaled_mm (cuBLASLt) FP8 e4m3 x e4m3 -> bf16, per-tensor scales, "
+                        "pre-quantized operands, same (M, N, K) as fwd / dgrad / wgrad"}
+    except Exception as e:  # no FP8 GEMM in this torch build or on this device
+        return {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 _INPUTS = {}
 
@@ -412,6 +474,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the layer-API leg and the cuBLASLt FP8 reference GEMMs")
     ap.add_argument("--serial-step", action="store_true",
                     help="capture the six launches on one stream instead of three")
     args = ap.parse_args()
@@ -548,6 +612,13 @@ def main():
                "steps": k_e2e, "ms_per_step": t_e2e / k_e2e * 1e3,
                "pipeline": "double-buffered: upload of step i+1 and download of step i-1 overlap step i's compute"}
 
+    extra = {}
+    if not args.no_extra:
+        extra["layer"] = layer_leg(step, stream)
+        extra["fp8_cublaslt_reference"] = fp8_reference_leg(dev, stream)
+        if m.device_status() != 0:
+            raise RuntimeError("device status word set in the layer leg")
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         nthreads = cpu_threads()
@@ -570,6 +641,7 @@ def main():
                                         f"dense fp4/bf16 ratio {NOMINAL_FP4_OVER_BF16:.0f}"},
             "breakdown": breakdown,
             "cpu_baseline": cpu,
+            **({"extra": extra} if extra else {}),
             "e2e": e2e,
             "gpu_launches": n_launch * args.steps,
             "timing": {"timed_region": ("CUDA-graph replay of the captured step, K times, CUDA events on the launch stream"

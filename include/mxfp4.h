@@ -82,6 +82,13 @@ int mxfp4_abi_version(void);
 /* Human-readable name of a status code (static string, never NULL). */
 const char* mxfp4_status_string(int status);
 
+/* The CUDA runtime error code behind the calling thread's most recent
+ * MXFP4_ERR_CUDA (0 if there was none), and the CUDA runtime's name for a
+ * code (static string).  No counterpart in the pages: a diagnostic for the
+ * one status that wraps another library's error. */
+int mxfp4_last_cuda_error(void);
+const char* mxfp4_cuda_error_string(int cuda_error);
+
 /* Bytes of codes for a [rows, cols] tensor quantized along cols: rows*cols/2. */
 size_t mxfp4_codes_bytes(int64_t rows, int64_t cols);
 

@@ -23,6 +23,7 @@ _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG_DIR, "libmxfp4.so")
 
 MXFP4_OK = 0
+MXFP4_ERR_CUDA = 5
 MXFP4_HADAMARD_ROW = 1
 MXFP4_HADAMARD_COL = 2
 MXFP4_SCALE_LINEAR = 4
@@ -33,7 +34,7 @@ ABI_SYMBOLS = (
     "mxfp4_abi_version", "mxfp4_status_string", "mxfp4_codes_bytes", "mxfp4_scales_bytes",
     "mxfp4_cast", "mxfp4_cast_dual", "gemm_fp4", "mxfp4_workspace_bytes",
     "gemm_fp4_bf16_fwd", "gemm_fp4_bf16_dgrad", "gemm_fp4_bf16_wgrad", "mxfp4_device_status",
-    "gemm_fp4_bf16_fwd_noalloc",
+    "gemm_fp4_bf16_fwd_noalloc", "mxfp4_last_cuda_error", "mxfp4_cuda_error_string",
 )
 
 _lib = None
@@ -43,7 +44,12 @@ _lock = threading.Lock()
 class Mxfp4Error(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {status_string(status)} ({status})")
+        self.cuda_error = 0
+        msg = f"{where}: {status_string(status)} ({status})"
+        if status == MXFP4_ERR_CUDA:
+            self.cuda_error = lib().mxfp4_last_cuda_error()
+            msg += f", CUDA error {self.cuda_error} ({lib().mxfp4_cuda_error_string(self.cuda_error).decode()})"
+        super().__init__(msg)
 
 
 def lib() -> ctypes.CDLL:
@@ -71,6 +77,8 @@ def lib() -> ctypes.CDLL:
                 "gemm_fp4_bf16_wgrad": (I, [P, P, P, I64, I64, I64, U32, P, SZ, P]),
                 "mxfp4_device_status": (I, [I, ctypes.POINTER(I)]),
                 "gemm_fp4_bf16_fwd_noalloc": (I, [P, P, P, I64, I64, I64, P]),
+                "mxfp4_last_cuda_error": (I, []),
+                "mxfp4_cuda_error_string": (ctypes.c_char_p, [I]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)

@@ -23,25 +23,55 @@ constexpr int64_t kMaxDim = int64_t(1) << 31;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// The current device must be compute capability 10.3.  The answer per device
-// is cached (it cannot change within a process): 0 unknown, 1 yes, 2 no.
-mxfp4_status check_device() {
+// The CUDA error behind this thread's last MXFP4_ERR_CUDA.
+thread_local int t_last_cuda_error = 0;
+
+mxfp4_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return MXFP4_OK;
+  t_last_cuda_error = static_cast<int>(e);
+  return MXFP4_ERR_CUDA;
+}
+
+}  // namespace
+
+// This library links its own CUDA runtime, whose per-thread current device is
+// separate from the caller's (torch's) runtime: a thread that torch created
+// (an autograd worker, say) may have no current context here at all, and
+// the tensor-map encode is a driver call that needs one.  So every entry
+// point makes the device that holds its data current in this runtime, which
+// also binds that device's primary context to the calling thread.
+cudaError_t mxfp4::bind_device_of(const void* data) {
+  cudaPointerAttributes attr{};
+  cudaError_t e = cudaPointerGetAttributes(&attr, data);
+  if (e != cudaSuccess) return e;
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return cudaErrorInvalidValue;
+  return cudaSetDevice(attr.device);
+}
+
+namespace {
+
+// Binds the data's device (above), which must be compute capability 10.3.
+// The answer per device is cached (it cannot change within a process):
+// 0 unknown, 1 yes, 2 no.
+mxfp4_status check_device(const void* data) {
   static std::atomic<int> known[64];
+  cudaError_t e = mxfp4::bind_device_of(data);
+  if (e == cudaErrorInvalidValue) return MXFP4_ERR_INVALID_ARG;  // not device memory
+  if (e != cudaSuccess) return from_cuda(e);
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MXFP4_ERR_CUDA;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e);
   int k = (dev >= 0 && dev < 64) ? known[dev].load(std::memory_order_relaxed) : 0;
   if (k == 0) {
     int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return MXFP4_ERR_CUDA;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return from_cuda(e);
     k = (major == 10 && minor == 3) ? 1 : 2;
     if (dev >= 0 && dev < 64) known[dev].store(k, std::memory_order_relaxed);
   }
   return k == 1 ? MXFP4_OK : MXFP4_ERR_UNSUPPORTED_DEVICE;
 }
-
-mxfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -110,6 +140,12 @@ extern "C" {
 
 int mxfp4_abi_version(void) { return 1; }
 
+int mxfp4_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* mxfp4_cuda_error_string(int cuda_error) {
+  return cudaGetErrorName(static_cast<cudaError_t>(cuda_error));
+}
+
 const char* mxfp4_status_string(int status) {
   switch (status) {
     case MXFP4_OK: return "MXFP4_OK";
@@ -142,7 +178,7 @@ mxfp4_status mxfp4_cast(const uint16_t* x, int64_t rows, int64_t cols, int64_t l
   if (rows == 0 || cols == 0) return MXFP4_OK;
   MXFP4_TRY(check_out(q));
   MXFP4_TRY(check_out(sf));
-  MXFP4_TRY(check_device());
+  MXFP4_TRY(check_device(x));
   CastArgs a{x, rows, cols, ldx, q, sf, nullptr, nullptr, flags};
   return from_cuda(mxfp4::launch_cast(a, static_cast<cudaStream_t>(stream)));
 }
@@ -159,7 +195,7 @@ mxfp4_status mxfp4_cast_dual(const uint16_t* x, int64_t rows, int64_t cols, int6
   MXFP4_TRY(check_out(sf_row));
   MXFP4_TRY(check_out(q_col));
   MXFP4_TRY(check_out(sf_col));
-  MXFP4_TRY(check_device());
+  MXFP4_TRY(check_device(x));
   CastArgs a{x, rows, cols, ldx, q_row, sf_row, q_col, sf_col, flags};
   return from_cuda(mxfp4::launch_cast(a, static_cast<cudaStream_t>(stream)));
 }
@@ -178,7 +214,7 @@ mxfp4_status gemm_fp4(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, c
     MXFP4_TRY(check_out(b));
     MXFP4_TRY(check_out(b_sf));
   }
-  MXFP4_TRY(check_device());
+  MXFP4_TRY(check_device(c));
   return gemm_checked(a, a_sf, b, b_sf, c, M, N, K, ldc, static_cast<cudaStream_t>(stream));
 }
 
@@ -201,7 +237,7 @@ mxfp4_status gemm_fp4_bf16_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y
   if (N % 8 != 0) return MXFP4_ERR_MISALIGNED;
   if (ws == nullptr || ws_bytes < mxfp4_workspace_bytes(MXFP4_OP_FWD, M, N, K) || !aligned16(ws))
     return MXFP4_ERR_WORKSPACE;
-  MXFP4_TRY(check_device());
+  MXFP4_TRY(check_device(y));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return from_cuda(mxfp4::launch_fill_zero_bf16(y, M, N, N, s));
   uint8_t* cur = static_cast<uint8_t*>(ws);
@@ -222,7 +258,7 @@ mxfp4_status gemm_fp4_bf16_dgrad(const uint16_t* dy, const uint16_t* w, uint16_t
   MXFP4_TRY(check_out(dx));
   if (ws == nullptr || ws_bytes < mxfp4_workspace_bytes(MXFP4_OP_DGRAD, M, N, K) || !aligned16(ws))
     return MXFP4_ERR_WORKSPACE;
-  MXFP4_TRY(check_device());
+  MXFP4_TRY(check_device(dx));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (N == 0) return from_cuda(mxfp4::launch_fill_zero_bf16(dx, M, K, K, s));
   uint8_t* cur = static_cast<uint8_t*>(ws);
@@ -245,7 +281,7 @@ mxfp4_status gemm_fp4_bf16_wgrad(const uint16_t* dy, const uint16_t* x, uint16_t
   MXFP4_TRY(check_out(dw));
   if (ws == nullptr || ws_bytes < mxfp4_workspace_bytes(MXFP4_OP_WGRAD, M, N, K) || !aligned16(ws))
     return MXFP4_ERR_WORKSPACE;
-  MXFP4_TRY(check_device());
+  MXFP4_TRY(check_device(dw));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M == 0) return from_cuda(mxfp4::launch_fill_zero_bf16(dw, N, K, K, s));
   uint8_t* cur = static_cast<uint8_t*>(ws);

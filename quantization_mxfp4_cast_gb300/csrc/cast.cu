@@ -506,10 +506,14 @@ cudaError_t launch_cast_t(const CUtensorMap& tm, const CastArgs& args, int col_t
   }
   int* status = device_status_word();
   if (status == nullptr) return cudaErrorUnknown;
-  const int grid = std::min(num_tiles, per_sm);
-  cast_kernel<kRow, kCol><<<grid, kThreads, kCastSmemBytes, stream>>>(tm, args, col_tiles, num_tiles,
-                                                                     status);
-  return cudaGetLastError();
+  // cudaLaunchKernelEx reports this launch's own error; the thread's last
+  // error may hold a stale, unrelated one (e.g. a not-ready query result).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min(num_tiles, per_sm)), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kCastSmemBytes;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, cast_kernel<kRow, kCol>, tm, args, col_tiles, num_tiles, status);
 }
 
 }  // namespace

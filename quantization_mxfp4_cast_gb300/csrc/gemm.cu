@@ -499,8 +499,11 @@ cudaError_t launch_fill_zero_bf16(uint16_t* c, int64_t M, int64_t N, int64_t ldc
   if (M == 0 || N == 0) return cudaSuccess;
   const int64_t total = M * N;
   const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, 152 * 8));
-  fill_zero_bf16_kernel<<<blocks, 256, 0, stream>>>(c, M, N, ldc);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, fill_zero_bf16_kernel, c, M, N, ldc);
 }
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream) {
@@ -543,9 +546,8 @@ cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel, tmA, tmB, tmSfa, tmSfb, tmC, p);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  // the launch's own result (the thread's last error may be stale and unrelated)
+  return cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel, tmA, tmB, tmSfa, tmSfb, tmC, p);
 }
 
 }  // namespace mxfp4

@@ -24,6 +24,11 @@ struct CastArgs {
 // One launch over 128 x 128 tiles of x; writes whichever outputs are non-null.
 cudaError_t launch_cast(const CastArgs& args, cudaStream_t stream);
 
+// Makes the device that holds `data` current in this library's CUDA runtime
+// for the calling thread (binding its primary context); cudaErrorInvalidValue
+// if `data` is not device memory.
+cudaError_t bind_device_of(const void* data);
+
 struct GemmArgs {
   const uint8_t* a;     // codes [M, K/2]
   const uint8_t* a_sf;  // tiled scales, M rows x K/32 blocks

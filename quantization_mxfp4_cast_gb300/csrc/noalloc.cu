@@ -21,6 +21,7 @@
 #include <mutex>
 
 #include "../../include/mxfp4.h"
+#include "internal.h"
 
 namespace {
 
@@ -55,6 +56,12 @@ extern "C" mxfp4_status gemm_fp4_bf16_fwd_noalloc(const uint16_t* x, const uint1
                                                    void* stream) {
   if (M < 0 || N < 0 || K < 0) return MXFP4_ERR_INVALID_ARG;
   if (mxfp4_workspace_bytes(MXFP4_OP_FWD, M, N, K) > kScratchBytes) return MXFP4_ERR_WORKSPACE;
+  if (y == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (M > 0 && N > 0) {  // scratch of the device that holds the output
+    const cudaError_t e = mxfp4::bind_device_of(y);
+    if (e == cudaErrorInvalidValue) return MXFP4_ERR_INVALID_ARG;
+    if (e != cudaSuccess) return MXFP4_ERR_CUDA;
+  }
   void* scratch = nullptr;
   const mxfp4_status st = scratch_address(&scratch);
   if (st != MXFP4_OK) return st;

@@ -108,3 +108,8 @@ def test_argument_validation_before_any_launch(L):
     assert L.gemm_fp4_bf16_wgrad(good, good, good, 64, 64, 64, 1, good, 1 << 30, None) == INV
     st = ctypes.c_int(0)
     assert L.mxfp4_device_status(0, None) == INV
+
+
+def test_cuda_error_diagnostic(L):
+    assert L.mxfp4_last_cuda_error() == 0          # no CUDA failure in this thread yet
+    assert L.mxfp4_cuda_error_string(0) == b"cudaSuccess"

@@ -1,0 +1,107 @@
+"""GPU parity of the layer-level MXFP4 train step (MXFP4Linear: forward,
+dgrad and wgrad through the library's casts and GEMMs) against the fp64
+oracle, and the weight workspace's reuse of quantized weights.
+
+Method: jax-aiter README, "Supported ops" rows "FP4 GEMM (training)" (FP4
+forward, dA and dB with BF16 in/out) and "MXFP4 Quantizer / Workspace"
+(weight / activation / grad presets, quantized-weight cache by name);
+"Quick start" (grad_out cast with a Hadamard transform).  The Hadamard is on
+the column copies of both wgrad operands."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantization_mxfp4_cast_gb300 import synth
+from tests.util import bf16_bits, build_library, gemm_tolerance_ok
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_library()
+    from quantization_mxfp4_cast_gb300 import layer
+    return layer
+
+
+def oracle_step(x, w, dy):
+    """fp64 oracle of Y = X W^T, dX = dY W, dW = dY^T X through MXFP4 casts."""
+    cx, sx = oracle.cast_rows(bf16_bits(x))
+    cw, sw = oracle.cast_rows(bf16_bits(w))
+    y = oracle.gemm_mxfp4(cx, sx, cw, sw, nthreads=8)
+    cd, sd = oracle.cast_rows(bf16_bits(dy))
+    cwc, swc = oracle.cast_cols(bf16_bits(w))
+    dx = oracle.gemm_mxfp4(cd, sd, cwc, swc, nthreads=8)
+    cdc, sdc = oracle.cast_cols(bf16_bits(dy), hadamard=True)
+    cxc, sxc = oracle.cast_cols(bf16_bits(x), hadamard=True)
+    dw = oracle.gemm_mxfp4(cdc, sdc, cxc, sxc, nthreads=8)
+    return y, dx, dw
+
+
+def close(gpu, ref, what):
+    ok, excess = gemm_tolerance_ok(gpu.float().cpu().numpy(), ref)
+    assert ok, f"{what}: worst excess over tolerance {excess:.3e}"
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (160, 96, 320)])
+def test_linear_train_step_matches_oracle(L, M, N, K):
+    x, w, dy = synth.linear_layer(M, N, K, 1.0)
+    layer = L.MXFP4Linear(w.cuda(), cache_name="t")
+    xd = x.cuda().requires_grad_(True)
+    y = layer(xd)
+    y.backward(dy.cuda())
+    torch.cuda.synchronize()
+    ry, rdx, rdw = oracle_step(x, w, dy)
+    close(y.detach(), ry, "fwd")
+    close(xd.grad, rdx, "dgrad")
+    close(layer.weight.grad, rdw, "wgrad")
+
+
+def test_leading_dims_are_tokens(L):
+    M, N, K = 256, 128, 256
+    x, w, dy = synth.linear_layer(M, N, K, 1.0)
+    layer = L.MXFP4Linear(w.cuda())
+    x3 = x.cuda().reshape(2, M // 2, K).requires_grad_(True)
+    y3 = layer(x3)
+    assert y3.shape == (2, M // 2, N)
+    y3.backward(dy.cuda().reshape(2, M // 2, N))
+    torch.cuda.synchronize()
+    ry, rdx, rdw = oracle_step(x, w, dy)
+    close(y3.detach().reshape(M, N), ry, "fwd")
+    close(x3.grad.reshape(M, K), rdx, "dgrad")
+    close(layer.weight.grad, rdw, "wgrad")
+
+
+def test_workspace_reuses_until_the_weight_changes(L):
+    M, N, K = 128, 256, 256
+    x, w, _ = synth.linear_layer(M, N, K, 1.0)
+    layer = L.MXFP4Linear(w.cuda(), cache_name="w0")
+    xd = x.cuda()
+    with torch.no_grad():
+        y0 = layer(xd)
+        y1 = layer(xd)                                  # same weight: cached casts
+        assert layer.workspace.casts == 1
+        assert torch.equal(y0, y1)
+        layer.weight.mul_(-1.0)                         # in-place update bumps the version
+        y2 = layer(xd)
+    torch.cuda.synchronize()
+    assert layer.workspace.casts == 2
+    assert torch.equal(y2, -y0)                          # the sign flips exactly in MXFP4 too
+    cx, sx = oracle.cast_rows(bf16_bits(x))
+    cw, sw = oracle.cast_rows(bf16_bits(-w))
+    close(y2, oracle.gemm_mxfp4(cx, sx, cw, sw, nthreads=8), "fwd after update")
+
+
+def test_quantizer_presets_match_the_dual_cast(L):
+    t = synth.normal_bf16((256, 128), 1.0, seed=9)
+    for q, had in ((L.MXFP4Quantizer.for_weight(), False), (L.MXFP4Quantizer.for_activation(), True),
+                   (L.MXFP4Quantizer.for_grad(), True)):
+        tq = q.quantize(t.cuda())
+        torch.cuda.synchronize()
+        cr, sr = oracle.cast_rows(bf16_bits(t))
+        cc, sc = oracle.cast_cols(bf16_bits(t), hadamard=had)
+        assert np.array_equal(tq.q_row.cpu().numpy(), cr)
+        assert np.array_equal(tq.sf_row.cpu().numpy(), oracle.sf_linear_to_tile(sr))
+        assert np.array_equal(tq.q_col.cpu().numpy(), cc)
+        assert np.array_equal(tq.sf_col.cpu().numpy(), oracle.sf_linear_to_tile(sc))
