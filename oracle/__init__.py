@@ -78,6 +78,18 @@ def _load():
             lib.oracle_dequant_rows.restype = ctypes.c_int
             lib.oracle_gemm_abt_f64.argtypes = [P, P, I64, I64, I64, P, ctypes.c_int]
             lib.oracle_gemm_abt_f64.restype = ctypes.c_int
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_int]
+            lib.oracle_e4m3_value.restype = ctypes.c_double
+            lib.oracle_e4m3_magnitude_code.argtypes = [ctypes.c_double]
+            lib.oracle_e4m3_magnitude_code.restype = ctypes.c_int
+            lib.oracle_block_exponent_e4m3.argtypes = [ctypes.c_double]
+            lib.oracle_block_exponent_e4m3.restype = ctypes.c_int
+            for name in ("oracle_cast_rows_mxfp8", "oracle_cast_cols_mxfp8"):
+                f = getattr(lib, name)
+                f.argtypes = [P, I64, I64, I64, ctypes.c_int, P, P]
+                f.restype = ctypes.c_int
+            lib.oracle_dequant_rows_mxfp8.argtypes = [P, P, I64, I64, P]
+            lib.oracle_dequant_rows_mxfp8.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -176,6 +188,63 @@ def gemm_mxfp4(codes_a, sf_a, codes_b, sf_b, nthreads: int = 1) -> np.ndarray:
     """fp64 C = dequant(A) . dequant(B)^T for row-wise MXFP4 operands with
     linear scales (A: [M, K/2] codes, [M, K/32] scales; B likewise, [N, ...])."""
     return gemm_abt(dequant_rows(codes_a, sf_a), dequant_rows(codes_b, sf_b), nthreads)
+
+
+# --------------------------------------------------------------------------- MXFP8 (E4M3)
+def e4m3_value(code: int) -> float:
+    return _load().oracle_e4m3_value(int(code))
+
+
+def e4m3_magnitude_code(u: float) -> int:
+    return _load().oracle_e4m3_magnitude_code(float(u))
+
+
+def block_exponent_e4m3(amax: float) -> int:
+    return _load().oracle_block_exponent_e4m3(float(amax))
+
+
+def cast_rows_mxfp8(x, hadamard: bool = False):
+    """Row-wise MXFP8 cast of bf16 x[rows, cols] -> (codes [rows, cols] u8,
+    scales [rows, cols/32] u8, linear layout)."""
+    xb = np.ascontiguousarray(as_bf16_bits(x))
+    rows, cols = xb.shape
+    codes = np.zeros((rows, cols), dtype=np.uint8)
+    scales = np.zeros((rows, cols // 32), dtype=np.uint8)
+    rc = _load().oracle_cast_rows_mxfp8(_ptr(xb), rows, cols, cols, int(bool(hadamard)), _ptr(codes),
+                                        _ptr(scales))
+    if rc != 0:
+        raise ValueError("cols must be a multiple of 32")
+    return codes, scales
+
+
+def cast_cols_mxfp8(x, hadamard: bool = False):
+    """Column-wise (transposed) MXFP8 cast -> (codes [cols, rows], scales [cols, rows/32])."""
+    xb = np.ascontiguousarray(as_bf16_bits(x))
+    rows, cols = xb.shape
+    codes = np.zeros((cols, rows), dtype=np.uint8)
+    scales = np.zeros((cols, rows // 32), dtype=np.uint8)
+    rc = _load().oracle_cast_cols_mxfp8(_ptr(xb), rows, cols, cols, int(bool(hadamard)), _ptr(codes),
+                                        _ptr(scales))
+    if rc != 0:
+        raise ValueError("rows must be a multiple of 32")
+    return codes, scales
+
+
+def dequant_rows_mxfp8(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    rows, cols = codes.shape
+    out = np.empty((rows, cols), dtype=np.float64)
+    rc = _load().oracle_dequant_rows_mxfp8(_ptr(codes), _ptr(scales), rows, cols, _ptr(out))
+    if rc != 0:
+        raise ValueError("bad shape")
+    return out
+
+
+def gemm_mxfp8(codes_a, sf_a, codes_b, sf_b, nthreads: int = 1) -> np.ndarray:
+    """fp64 C = dequant(A) . dequant(B)^T for row-wise MXFP8 operands
+    (A: [M, K] codes, [M, K/32] scales; B: [N, K], [N, K/32])."""
+    return gemm_abt(dequant_rows_mxfp8(codes_a, sf_a), dequant_rows_mxfp8(codes_b, sf_b), nthreads)
 
 
 # --------------------------------------------------------------------------- scale tile layout

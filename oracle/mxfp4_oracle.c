@@ -236,3 +236,130 @@ int oracle_gemm_abt_f64(const double* a, const double* b, int64_t m, int64_t n, 
         if (running[t]) pthread_join(tid[t], NULL);
     return 0;
 }
+
+/*
+ * MXFP8 (E4M3 elements, E8M0 block scales): the FP8 alternative for the wgrad
+ * operands.  Method: jax-aiter README, "MXFP4 training architecture" (an FP8
+ * dB path next to the FP4 one).  The pages fix nothing about it; the readings
+ * (listed in the design notes) follow the OCP MX rules as above:
+ *   - E4M3: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is
+ *     subnormal (m * 2^-9); magnitude code 0x7F is NaN, so the largest
+ *     finite magnitude is 0x7E = 1.75 * 2^8 = 448;
+ *   - e = floor(log2(amax)) - 8 (8 = the exponent of E4M3's largest normal),
+ *     clamped to [-127, 127], byte e + 127; all-zero block: byte 0x00;
+ *     NaN or infinity in the block: byte 0xFF and codes 0;
+ *   - v = x * 2^-e rounded to the nearest E4M3 value, ties to the even code,
+ *     |v| >= 448 saturating to 448; the sign is kept; one byte per element.
+ */
+
+/* Magnitude of the 7-bit E4M3 magnitude code m (0..126); NaN for 127. */
+static double e4m3_magnitude(int m) {
+    if (m >= 127) return NAN;
+    int ex = m >> 3, mant = m & 7;
+    if (ex == 0) return ldexp((double)mant, -9);
+    return ldexp(1.0 + mant / 8.0, ex - 7);
+}
+
+double oracle_e4m3_value(int code) {
+    double v = e4m3_magnitude(code & 0x7F);
+    return (code & 0x80) ? -v : v;
+}
+
+/* Magnitude code of u >= 0: the nearest of the 127 finite magnitudes, found by
+ * trying them all; on a tie the even code wins.  u >= 448 gives 0x7E. */
+int oracle_e4m3_magnitude_code(double u) {
+    if (u >= 448.0) return 0x7E;
+    int best = 0;
+    double best_d = fabs(u - e4m3_magnitude(0));
+    for (int c = 1; c < 127; ++c) {
+        double d = fabs(u - e4m3_magnitude(c));
+        if (d < best_d || (d == best_d && (c % 2) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return best;
+}
+
+/* Shared exponent for E4M3 elements: floor(log2 amax) - 8, clamped. */
+int oracle_block_exponent_e4m3(double amax) {
+    if (amax == 0.0) return -127;
+    int p = 0;
+    (void)frexp(amax, &p);
+    int e = (p - 1) - 8;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+/* One block of 32 fp32 values -> 32 code bytes; returns the scale byte. */
+static uint8_t quantize_block_e4m3(const float* y, uint8_t* codes32) {
+    int nonfinite = 0;
+    double amax = 0.0;
+    for (int i = 0; i < BLOCK; ++i) {
+        if (isnan(y[i]) || isinf(y[i])) nonfinite = 1;
+        double a = fabs((double)y[i]);
+        if (a > amax) amax = a;
+    }
+    if (nonfinite) {
+        memset(codes32, 0, BLOCK);
+        return 0xFF;
+    }
+    int e = oracle_block_exponent_e4m3(amax);
+    for (int i = 0; i < BLOCK; ++i) {
+        double v = ldexp((double)y[i], -e);
+        int code = oracle_e4m3_magnitude_code(fabs(v));
+        if (signbit(y[i])) code |= 0x80;
+        codes32[i] = (uint8_t)code;
+    }
+    return (uint8_t)(e + 127);
+}
+
+/* Row-wise MXFP8 cast: codes [rows, cols] (one byte per element), scales
+ * [rows, cols/32]; hadamard != 0 transforms every block first (fp32, as
+ * above).  Returns -1 if cols is not a multiple of 32. */
+int oracle_cast_rows_mxfp8(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, int hadamard,
+                           uint8_t* codes, uint8_t* scales) {
+    if (cols % BLOCK != 0) return -1;
+    const int64_t nb = cols / BLOCK;
+    float y[BLOCK];
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            for (int i = 0; i < BLOCK; ++i) y[i] = bf16_to_float(x[r * ldx + b * BLOCK + i]);
+            if (hadamard) oracle_fwht32_f32(y);
+            scales[r * nb + b] = quantize_block_e4m3(y, codes + r * cols + b * BLOCK);
+        }
+    }
+    return 0;
+}
+
+/* Column-wise (transposed) MXFP8 cast: the row-wise cast of x^T.
+ * codes [cols, rows], scales [cols, rows/32]. */
+int oracle_cast_cols_mxfp8(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, int hadamard,
+                           uint8_t* codes, uint8_t* scales) {
+    if (rows % BLOCK != 0) return -1;
+    const int64_t nb = rows / BLOCK;
+    float y[BLOCK];
+    for (int64_t c = 0; c < cols; ++c) {
+        for (int64_t b = 0; b < nb; ++b) {
+            for (int i = 0; i < BLOCK; ++i) y[i] = bf16_to_float(x[(b * BLOCK + i) * ldx + c]);
+            if (hadamard) oracle_fwht32_f32(y);
+            scales[c * nb + b] = quantize_block_e4m3(y, codes + c * rows + b * BLOCK);
+        }
+    }
+    return 0;
+}
+
+/* out[r, k] = e4m3(code) * 2^(scale - 127); NaN for scale byte 0xFF. */
+int oracle_dequant_rows_mxfp8(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols,
+                              double* out) {
+    if (cols % BLOCK != 0) return -1;
+    const int64_t nb = cols / BLOCK;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t k = 0; k < cols; ++k) {
+            uint8_t s = scales[r * nb + k / BLOCK];
+            out[r * cols + k] = (s == 0xFF) ? NAN : ldexp(oracle_e4m3_value(codes[r * cols + k]), (int)s - 127);
+        }
+    }
+    return 0;
+}
