@@ -327,6 +327,30 @@ def layer_leg(step, stream, iters=10):
                     "in a WeightWorkspace across micro-batches"}
 
 
+def fp8_wgrad_leg(step, stream, iters=20):
+    """The FP8 alternative for the step's wgrad (dW = dY^T X over the tokens):
+    MXFP8 (E4M3) column casts of dY and X with the Hadamard, then the
+    kind::mxf8f6f4 GEMM, each timed on its own (CUDA events, back to back)."""
+    m = step.m
+    with torch.cuda.stream(stream):
+        qdy = m.mxfp8_cast_cols(step.dy, hadamard=True, stream=stream)
+        qx = m.mxfp8_cast_cols(step.x, hadamard=True, stream=stream)
+        dw = torch.empty(N, K, dtype=torch.bfloat16, device=step.x.device)
+        t_cast_dy = time_loop(lambda: m.mxfp8_cast_cols(step.dy, hadamard=True, out=qdy, stream=stream),
+                              iters, 3, stream)
+        t_cast_x = time_loop(lambda: m.mxfp8_cast_cols(step.x, hadamard=True, out=qx, stream=stream),
+                             iters, 3, stream)
+        t_gemm = time_loop(lambda: m.gemm_mxfp8(qdy[0], qdy[1], qx[0], qx[1], N, K, M, c=dw, stream=stream),
+                           iters, 3, stream)
+    cast_bytes = lambda r, c: r * c * (2 + 1) + r * c // 32  # bf16 in, E4M3 codes + scales out
+    return {"gemm_tflops": 2.0 * M * N * K / t_gemm / 1e12, "gemm_us": t_gemm * 1e6,
+            "cast_gbs": {"dY": cast_bytes(M, N) / t_cast_dy / 1e9, "X": cast_bytes(M, K) / t_cast_x / 1e9},
+            "cast_us": {"dY": t_cast_dy * 1e6, "X": t_cast_x * 1e6},
+            "wgrad_tflops_with_casts": 2.0 * M * N * K / (t_gemm + t_cast_dy + t_cast_x) / 1e12,
+            "what": "MXFP8 wgrad recipe: column casts of dY and X (E4M3 + E8M0, Hadamard along M) "
+                    "and the kind::mxf8f6f4 GEMM dW[N,K] = dY^T X"}
+
+
 def fp8_reference_leg(dev, stream, iters=20):
     """cuBLASLt FP8 (e4m3, per-tensor scales, bf16 out) through torch._scaled_mm
     on the step's three GEMM shapes, operands pre-quantized: context for the
@@ -615,6 +639,7 @@ def main():
     extra = {}
     if not args.no_extra:
         extra["layer"] = layer_leg(step, stream)
+        extra["mxfp8_wgrad"] = fp8_wgrad_leg(step, stream)
         extra["fp8_cublaslt_reference"] = fp8_reference_leg(dev, stream)
         if m.device_status() != 0:
             raise RuntimeError("device status word set in the layer leg")

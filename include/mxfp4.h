@@ -75,6 +75,7 @@ typedef enum {
 #define MXFP4_OP_FWD 0
 #define MXFP4_OP_DGRAD 1
 #define MXFP4_OP_WGRAD 2
+#define MXFP4_OP_WGRAD_FP8 3 /* gemm_fp8_bf16_wgrad */
 
 /* Version of this ABI (bumped on any signature change). */
 int mxfp4_abi_version(void);
@@ -133,6 +134,42 @@ mxfp4_status mxfp4_cast_dual(const uint16_t* x, int64_t rows, int64_t cols, int6
  */
 mxfp4_status gemm_fp4(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, const uint8_t* b_sf,
                       uint16_t* c, int64_t M, int64_t N, int64_t K, int64_t ldc, void* stream);
+
+/*
+ * MXFP8: the FP8 alternative for the wgrad operands (jax-aiter README,
+ * "MXFP4 training architecture": an FP8 dB path next to the FP4 one).
+ * E4M3 elements (one byte each, round to nearest even, saturating at 448)
+ * with the same E8M0 scales per 32 elements, scale byte
+ * floor(log2 amax) - 8 + 127 (clamped), the same NaN/Inf, zero-block and
+ * tile-layout conventions as MXFP4.
+ *
+ * mxfp8_cast_cols -- column-wise (transposed) MXFP8 cast of bf16 x[rows, cols]
+ * (row pitch ldx elements): q_col [cols, rows] bytes, sf_col scales of the
+ * [cols, rows/32] blocks (tile layout, or linear with MXFP4_SCALE_LINEAR).
+ * flags: MXFP4_HADAMARD_COL, MXFP4_SCALE_LINEAR.  rows, cols % 32 == 0.
+ */
+mxfp4_status mxfp8_cast_cols(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
+                             uint8_t* q_col, uint8_t* sf_col, uint32_t flags, void* stream);
+
+/*
+ * gemm_mxfp8 -- C[M,N] = A[M,K] . B[N,K]^T on MXFP8 operands, bf16 output:
+ *   a, a_sf : codes [M, K] bytes, scales (tile layout, M rows, K/32 blocks)
+ *   b, b_sf : codes [N, K] bytes, scales (tile layout, N rows, K/32 blocks)
+ *   c       : out, bf16 [M, N], row pitch ldc (ldc >= N, ldc % 8 == 0)
+ * Requires K % 32 == 0; M*N == 0 is a no-op; K == 0 writes zeros.
+ */
+mxfp4_status gemm_mxfp8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, const uint8_t* b_sf,
+                        uint16_t* c, int64_t M, int64_t N, int64_t K, int64_t ldc, void* stream);
+
+/*
+ * gemm_fp8_bf16_wgrad -- dW[N,K] = dY[M,N]^T . X[M,K] like gemm_fp4_bf16_wgrad,
+ * with both operands cast to MXFP8 along M (column-wise) into `ws`
+ * (mxfp4_workspace_bytes(MXFP4_OP_WGRAD_FP8, M, N, K) bytes).
+ * flags: MXFP4_HADAMARD_COL (both operands).  M % 32 == 0.
+ */
+mxfp4_status gemm_fp8_bf16_wgrad(const uint16_t* dy, const uint16_t* x, uint16_t* dw, int64_t M,
+                                 int64_t N, int64_t K, uint32_t flags, void* ws, size_t ws_bytes,
+                                 void* stream);
 
 /* Workspace bytes that gemm_fp4_bf16_{fwd,dgrad,wgrad} (op = MXFP4_OP_*)
  * need for the quantized copies of their operands; 0 for a bad op. */

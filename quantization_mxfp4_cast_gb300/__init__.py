@@ -27,7 +27,7 @@ MXFP4_ERR_CUDA = 5
 MXFP4_HADAMARD_ROW = 1
 MXFP4_HADAMARD_COL = 2
 MXFP4_SCALE_LINEAR = 4
-MXFP4_OP_FWD, MXFP4_OP_DGRAD, MXFP4_OP_WGRAD = 0, 1, 2
+MXFP4_OP_FWD, MXFP4_OP_DGRAD, MXFP4_OP_WGRAD, MXFP4_OP_WGRAD_FP8 = 0, 1, 2, 3
 
 # Every extern "C" symbol declared in include/mxfp4.h.
 ABI_SYMBOLS = (
@@ -35,6 +35,7 @@ ABI_SYMBOLS = (
     "mxfp4_cast", "mxfp4_cast_dual", "gemm_fp4", "mxfp4_workspace_bytes",
     "gemm_fp4_bf16_fwd", "gemm_fp4_bf16_dgrad", "gemm_fp4_bf16_wgrad", "mxfp4_device_status",
     "gemm_fp4_bf16_fwd_noalloc", "mxfp4_last_cuda_error", "mxfp4_cuda_error_string",
+    "mxfp8_cast_cols", "gemm_mxfp8", "gemm_fp8_bf16_wgrad",
 )
 
 _lib = None
@@ -78,6 +79,9 @@ def lib() -> ctypes.CDLL:
                 "mxfp4_device_status": (I, [I, ctypes.POINTER(I)]),
                 "gemm_fp4_bf16_fwd_noalloc": (I, [P, P, P, I64, I64, I64, P]),
                 "mxfp4_last_cuda_error": (I, []),
+                "mxfp8_cast_cols": (I, [P, I64, I64, I64, P, P, U32, P]),
+                "gemm_mxfp8": (I, [P, P, P, P, P, I64, I64, I64, I64, P]),
+                "gemm_fp8_bf16_wgrad": (I, [P, P, P, I64, I64, I64, U32, P, SZ, P]),
                 "mxfp4_cuda_error_string": (ctypes.c_char_p, [I]),
             }
             for name, (res, args) in sig.items():
@@ -229,6 +233,50 @@ def gemm_fp4_bf16_wgrad(dy, x, hadamard: bool = True, dw=None, ws=None, stream=N
     flags = MXFP4_HADAMARD_COL if hadamard else 0
     _check(lib().gemm_fp4_bf16_wgrad(_ptr(dy), _ptr(x), _ptr(dw), M, N, K, flags, _ptr(ws), nb,
                                      _stream(stream)), "gemm_fp4_bf16_wgrad")
+    return dw
+
+
+# ----------------------------------------------------------------------------- MXFP8 (wgrad alternative)
+def mxfp8_cast_cols(x, hadamard: bool = False, linear_scales: bool = False, out=None, stream=None):
+    """Column-wise (transposed) MXFP8 cast of bf16 x[R, C] -> (codes uint8 [C, R]
+    (E4M3, one byte per element), scales)."""
+    _bf16_2d(x, "x")
+    _need_cuda(x)
+    R, C = x.shape
+    if out is None:
+        out = (torch.empty(C, R, dtype=torch.uint8, device=x.device),
+               torch.empty(scales_bytes(C, R, linear_scales), dtype=torch.uint8, device=x.device))
+    q, sf = out
+    flags = (MXFP4_HADAMARD_COL if hadamard else 0) | (MXFP4_SCALE_LINEAR if linear_scales else 0)
+    _check(lib().mxfp8_cast_cols(_ptr(x), R, C, x.stride(0), _ptr(q), _ptr(sf), flags, _stream(stream)),
+           "mxfp8_cast_cols")
+    return q, sf
+
+
+def gemm_mxfp8(a, a_sf, b, b_sf, M: int, N: int, K: int, c=None, stream=None):
+    """C[M,N] (bf16) = A . B^T for MXFP8 operands (codes [M, K] / [N, K] bytes,
+    tile-layout scales)."""
+    _need_cuda(a, a_sf, b, b_sf)
+    if c is None:
+        c = torch.empty(M, N, dtype=torch.bfloat16, device=a.device)
+    _check(lib().gemm_mxfp8(_ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), _ptr(c), M, N, K, c.stride(0),
+                            _stream(stream)), "gemm_mxfp8")
+    return c
+
+
+def gemm_fp8_bf16_wgrad(dy, x, hadamard: bool = True, dw=None, ws=None, stream=None):
+    """dW[N,K] = dY[M,N]^T . X[M,K] with both operands cast to MXFP8 along the
+    tokens M (the FP8 alternative to gemm_fp4_bf16_wgrad)."""
+    _bf16_2d(dy, "dy"), _bf16_2d(x, "x")
+    _need_cuda(dy, x)
+    M, N = dy.shape
+    K = x.shape[1]
+    if dw is None:
+        dw = torch.empty(N, K, dtype=torch.bfloat16, device=dy.device)
+    ws, nb = _workspace(MXFP4_OP_WGRAD_FP8, M, N, K, ws, dy.device)
+    flags = MXFP4_HADAMARD_COL if hadamard else 0
+    _check(lib().gemm_fp8_bf16_wgrad(_ptr(dy), _ptr(x), _ptr(dw), M, N, K, flags, _ptr(ws), nb,
+                                     _stream(stream)), "gemm_fp8_bf16_wgrad")
     return dw
 
 

@@ -125,11 +125,26 @@ size_t carve_bytes(int64_t rows, int64_t cols) {
          align256(tile_scale_bytes(rows, cols));
 }
 
+// MXFP8 operand in the workspace: codes [rows, cols] bytes, tile scales.
+QuantView carve_fp8(uint8_t*& cursor, int64_t rows, int64_t cols) {
+  QuantView v;
+  v.q = cursor;
+  cursor += align256(static_cast<size_t>(rows) * static_cast<size_t>(cols));
+  v.sf = cursor;
+  cursor += align256(tile_scale_bytes(rows, cols));
+  return v;
+}
+
+size_t carve_fp8_bytes(int64_t rows, int64_t cols) {
+  return align256(static_cast<size_t>(rows) * static_cast<size_t>(cols)) +
+         align256(tile_scale_bytes(rows, cols));
+}
+
 mxfp4_status gemm_checked(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
                           const uint8_t* b_sf, uint16_t* c, int64_t M, int64_t N, int64_t K,
-                          int64_t ldc, cudaStream_t s) {
+                          int64_t ldc, cudaStream_t s, bool fp8 = false) {
   GemmArgs g{a, a_sf, b, b_sf, c, M, N, K, ldc};
-  cudaError_t e = mxfp4::launch_gemm(g, s);
+  cudaError_t e = fp8 ? mxfp4::launch_gemm_mxfp8(g, s) : mxfp4::launch_gemm(g, s);
   if (e == cudaErrorInvalidValue) return MXFP4_ERR_INVALID_ARG;
   return from_cuda(e);
 }
@@ -218,9 +233,65 @@ mxfp4_status gemm_fp4(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, c
   return gemm_checked(a, a_sf, b, b_sf, c, M, N, K, ldc, static_cast<cudaStream_t>(stream));
 }
 
+mxfp4_status gemm_mxfp8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, const uint8_t* b_sf,
+                        uint16_t* c, int64_t M, int64_t N, int64_t K, int64_t ldc, void* stream) {
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return MXFP4_ERR_INVALID_ARG;
+  if (K % 32 != 0 || ldc < N) return MXFP4_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return MXFP4_OK;
+  MXFP4_TRY(check_out(c));
+  if (ldc % 8 != 0) return MXFP4_ERR_MISALIGNED;
+  if (K > 0) {
+    MXFP4_TRY(check_out(a));
+    MXFP4_TRY(check_out(a_sf));
+    MXFP4_TRY(check_out(b));
+    MXFP4_TRY(check_out(b_sf));
+  }
+  MXFP4_TRY(check_device(c));
+  return gemm_checked(a, a_sf, b, b_sf, c, M, N, K, ldc, static_cast<cudaStream_t>(stream), true);
+}
+
+mxfp4_status mxfp8_cast_cols(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
+                             uint8_t* q_col, uint8_t* sf_col, uint32_t flags, void* stream) {
+  if (flags & ~(MXFP4_HADAMARD_COL | MXFP4_SCALE_LINEAR)) return MXFP4_ERR_INVALID_ARG;
+  MXFP4_TRY(check_bf16_in(x, rows, cols, ldx));
+  if (rows % 32 != 0) return MXFP4_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return MXFP4_OK;
+  MXFP4_TRY(check_out(q_col));
+  MXFP4_TRY(check_out(sf_col));
+  MXFP4_TRY(check_device(x));
+  CastArgs a{x, rows, cols, ldx, nullptr, nullptr, q_col, sf_col, flags | mxfp4::kFlagFp8};
+  return from_cuda(mxfp4::launch_cast(a, static_cast<cudaStream_t>(stream)));
+}
+
+mxfp4_status gemm_fp8_bf16_wgrad(const uint16_t* dy, const uint16_t* x, uint16_t* dw, int64_t M,
+                                 int64_t N, int64_t K, uint32_t flags, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  if (flags & ~MXFP4_HADAMARD_COL) return MXFP4_ERR_INVALID_ARG;
+  MXFP4_TRY(check_bf16_in(dy, M, N, N));
+  MXFP4_TRY(check_bf16_in(x, M, K, K));
+  if (M % 32 != 0) return MXFP4_ERR_INVALID_ARG;
+  if (N == 0 || K == 0) return MXFP4_OK;
+  MXFP4_TRY(check_out(dw));
+  if (ws == nullptr || ws_bytes < mxfp4_workspace_bytes(MXFP4_OP_WGRAD_FP8, M, N, K) || !aligned16(ws))
+    return MXFP4_ERR_WORKSPACE;
+  MXFP4_TRY(check_device(dw));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M == 0) return from_cuda(mxfp4::launch_fill_zero_bf16(dw, N, K, K, s));
+  uint8_t* cur = static_cast<uint8_t*>(ws);
+  QuantView qdyt = carve_fp8(cur, N, M), qxt = carve_fp8(cur, K, M);
+  const uint32_t cf = ((flags & MXFP4_HADAMARD_COL) ? mxfp4::kFlagHadamardCol : 0u) | mxfp4::kFlagFp8;
+  CastArgs cdy{dy, M, N, N, nullptr, nullptr, qdyt.q, qdyt.sf, cf};  // dY^T along M
+  CastArgs cx{x, M, K, K, nullptr, nullptr, qxt.q, qxt.sf, cf};      // X^T along M
+  MXFP4_TRY(from_cuda(mxfp4::launch_cast(cdy, s)));
+  MXFP4_TRY(from_cuda(mxfp4::launch_cast(cx, s)));
+  return gemm_checked(qdyt.q, qdyt.sf, qxt.q, qxt.sf, dw, N, K, M, K, s, true);
+}
+
 size_t mxfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
   if (M < 0 || N < 0 || K < 0) return 0;
   switch (op) {
+    case MXFP4_OP_WGRAD_FP8: return carve_fp8_bytes(N, M) + carve_fp8_bytes(K, M);  // col(dY), col(X)
     case MXFP4_OP_FWD: return carve_bytes(M, K) + carve_bytes(N, K);    // row(X), row(W)
     case MXFP4_OP_DGRAD: return carve_bytes(M, N) + carve_bytes(K, N);  // row(dY), col(W)
     case MXFP4_OP_WGRAD: return carve_bytes(N, M) + carve_bytes(K, M);  // col(dY), col(X)

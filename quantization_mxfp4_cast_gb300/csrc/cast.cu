@@ -64,6 +64,35 @@ __device__ __forceinline__ uint32_t cvt8_e2m1(float v0, float v1, float v2, floa
   return out;
 }
 
+// E4M3 codes of 4 values, element 0 in the low byte.  The conversion rounds
+// to nearest even and saturates at +-448 (cvt puts its first source in the
+// upper byte, hence the swapped operands).
+__device__ __forceinline__ uint32_t cvt4_e4m3(float v0, float v1, float v2, float v3) {
+  uint32_t out;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(out)
+      : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+  return out;
+}
+
+// Code words of one 32-element block from an accessor v(i) of its scaled fp32
+// values: 4 words of E2M1 pairs (MXFP4) or 8 words of E4M3 bytes (MXFP8).
+template <bool kFp8, typename V>
+__device__ __forceinline__ void block_codes(V v, uint32_t* out) {
+  if constexpr (kFp8) {
+#pragma unroll
+    for (int g = 0; g < 8; ++g) out[g] = cvt4_e4m3(v(4 * g), v(4 * g + 1), v(4 * g + 2), v(4 * g + 3));
+  } else {
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      out[g] = cvt8_e2m1(v(8 * g), v(8 * g + 1), v(8 * g + 2), v(8 * g + 3), v(8 * g + 4), v(8 * g + 5),
+                         v(8 * g + 6), v(8 * g + 7));
+  }
+}
+
 // Elementwise max(|a|, |b|) of bf16 pairs, NaN-propagating (sign bits of
 // the result are the XOR of the inputs' and must be masked off).
 __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
@@ -102,8 +131,10 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
 
 // From the largest magnitude's bit pattern: scale byte and the exact
 // power-of-two multiplier 2^-e (as fp32, and as a bf16 bit pattern).  For a
-// finite amax with biased exponent E, floor(log2 amax) - 2 + 127 = E - 2,
-// clamped at 0 (E = 0 covers zero and subnormals).
+// finite amax with biased exponent E, floor(log2 amax) - kEmax + 127 =
+// E - kEmax, clamped at 0 (E = 0 covers zero and subnormals); kEmax is the
+// exponent of the element format's largest value (E2M1: 6 = 1.5 * 2^2 -> 2;
+// E4M3: 448 = 1.75 * 2^8 -> 8).
 struct BlockScale {
   uint32_t byte;
   float mult;
@@ -111,11 +142,12 @@ struct BlockScale {
   bool nonfinite;
 };
 
+template <int kEmax = 2>
 __device__ __forceinline__ BlockScale block_scale(uint32_t amax_bits) {
   BlockScale s;
   s.nonfinite = amax_bits >= 0x7F800000u;
   const int e_biased = static_cast<int>(amax_bits >> 23);
-  const int byte = e_biased > 2 ? e_biased - 2 : 0;
+  const int byte = e_biased > kEmax ? e_biased - kEmax : 0;
   s.mult = __uint_as_float(static_cast<uint32_t>(254 - byte) << 23);
   s.mult_bf16 = static_cast<uint32_t>(254 - byte) << 7;
   s.byte = s.nonfinite ? 0xFFu : static_cast<uint32_t>(byte);
@@ -214,7 +246,7 @@ constexpr int kTileBytes = 2 * kHalfBytes;
 constexpr int kSfTileBytes = 512;
 constexpr int kCastSmemBytes = 2 * kTileBytes + 4 * kSfTileBytes + 64 + 1024;
 
-template <bool kRow, bool kCol>
+template <bool kRow, bool kCol, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 3)
     cast_kernel(const __grid_constant__ CUtensorMap tmX, const CastArgs args, int col_tiles,
                 int num_tiles, int* status) {
@@ -274,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   uint8_t* sf_row_tile = sf_row_tiles + b * kSfTileBytes;
   uint8_t* sf_col_tile = sf_col_tiles + b * kSfTileBytes;
 
+  static_assert(!(kFp8 && kRow), "MXFP8 is produced column-wise only");
   // ---------------------------------------------------------------- row pass
   // One lane per 32-element block: warp w, lane l take tile row
   // 8 w + (l % 8) (+ 64 in the second iteration), block l / 8 of that row.
@@ -355,29 +388,18 @@ __global__ void __launch_bounds__(kThreads, 3)
     for (int i = 0; i < 32; ++i)
       w[i] = *reinterpret_cast<const uint32_t*>(colp + i * 128 + ((ch ^ (i & 7)) << 4));
     const bool rows_ok = r0 + rb * 32 < rows;  // rows is a multiple of 32
+    // MXFP4: 16 code bytes per column block; MXFP8 (E4M3, column output only): 32
+    constexpr int kWords = kFp8 ? 8 : 4;
+    constexpr int kEmax = kFp8 ? 8 : 2;
     BlockScale sa, sb;
-    uint4 ca, cb;  // codes of column 2p and 2p+1
+    uint32_t ca[kWords], cb[kWords];  // codes of column 2p and 2p+1
     if (!had) {
       const uint32_t m = tree_absmax_bf16x2<32>(w) & 0x7FFF7FFFu;
-      sa = block_scale(m << 16);
-      sb = block_scale(m & 0xFFFF0000u);
+      sa = block_scale<kEmax>(m << 16);
+      sb = block_scale<kEmax>(m & 0xFFFF0000u);
       const uint16_t ma = static_cast<uint16_t>(sa.mult_bf16), mb = static_cast<uint16_t>(sb.mult_bf16);
-      uint32_t* pa = &ca.x;
-      uint32_t* pb = &cb.x;
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const uint32_t* u = w + 8 * g;
-        pa[g] = cvt8_e2m1(bf16_times<false>(u[0], ma), bf16_times<false>(u[1], ma),
-                          bf16_times<false>(u[2], ma), bf16_times<false>(u[3], ma),
-                          bf16_times<false>(u[4], ma), bf16_times<false>(u[5], ma),
-                          bf16_times<false>(u[6], ma), bf16_times<false>(u[7], ma));
-        pb[g] = cvt8_e2m1(bf16_times<true>(u[0], mb), bf16_times<true>(u[1], mb),
-                          bf16_times<true>(u[2], mb), bf16_times<true>(u[3], mb),
-                          bf16_times<true>(u[4], mb), bf16_times<true>(u[5], mb),
-                          bf16_times<true>(u[6], mb), bf16_times<true>(u[7], mb));
-      }
-      if (sa.nonfinite) ca = make_uint4(0u, 0u, 0u, 0u);
-      if (sb.nonfinite) cb = make_uint4(0u, 0u, 0u, 0u);
+      block_codes<kFp8>([&](int i) { return bf16_times<false>(w[i], ma); }, ca);
+      block_codes<kFp8>([&](int i) { return bf16_times<true>(w[i], mb); }, cb);
     } else {
       // both columns through one 32-point butterfly network on fp32 pairs
       uint64_t y[32];
@@ -397,13 +419,16 @@ __global__ void __launch_bounds__(kThreads, 3)
       // |RN(h * c)| is RN(max |h| * c); the NaN-propagating max keeps NaN/Inf.
       const float ha = amax32([&](int i) { return lo2(y[i]); });
       const float hb = amax32([&](int i) { return hi2(y[i]); });
-      sa = block_scale(__float_as_uint(__fmul_rn(ha, kInvSqrt32)));
-      sb = block_scale(__float_as_uint(__fmul_rn(hb, kInvSqrt32)));
-      // v = RN(h * c) * 2^-e.  For scale bytes 3..250 this equals
-      // RN(h * (c * 2^-e)) exactly: c * 2^-e stays normal, and a transformed
-      // value RN(h * c) small enough to be subnormal gives |v| < 1/4, code 0
-      // either way.  Outside that range the two roundings are kept apart.
-      if ((sa.byte - 3u) <= 247u && (sb.byte - 3u) <= 247u) {
+      sa = block_scale<kEmax>(__float_as_uint(__fmul_rn(ha, kInvSqrt32)));
+      sb = block_scale<kEmax>(__float_as_uint(__fmul_rn(hb, kInvSqrt32)));
+      // v = RN(h * c) * 2^-e.  RN(h * (c * 2^-e)) is the same number when
+      // c * 2^-e stays normal (scale byte <= 250) and every transformed value
+      // RN(h * c) that is subnormal in fp32 (< 2^-126, so |v| < 2^(1 - byte))
+      // lands below the format's zero threshold either way: byte >= 3 for
+      // E2M1 (|v| < 1/4), byte >= 11 for E4M3 (|v| <= 2^-10).  Outside that
+      // range the two roundings are kept apart.
+      constexpr uint32_t kFusedMin = kFp8 ? 11u : 3u;
+      if ((sa.byte - kFusedMin) <= 250u - kFusedMin && (sb.byte - kFusedMin) <= 250u - kFusedMin) {
         const uint64_t m2 = pk2(__fmul_rn(kInvSqrt32, sa.mult), __fmul_rn(kInvSqrt32, sb.mult));
 #pragma unroll
         for (int i = 0; i < 32; ++i) y[i] = mul2(y[i], m2);
@@ -413,26 +438,29 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
         for (int i = 0; i < 32; ++i) y[i] = mul2(mul2(y[i], c2), m2);
       }
-      uint32_t* pa = &ca.x;
-      uint32_t* pb = &cb.x;
+      block_codes<kFp8>([&](int i) { return lo2(y[i]); }, ca);
+      block_codes<kFp8>([&](int i) { return hi2(y[i]); }, cb);
+    }
+    if (sa.nonfinite) {
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const uint64_t* u = y + 8 * g;
-        pa[g] = cvt8_e2m1(lo2(u[0]), lo2(u[1]), lo2(u[2]), lo2(u[3]), lo2(u[4]), lo2(u[5]),
-                          lo2(u[6]), lo2(u[7]));
-        pb[g] = cvt8_e2m1(hi2(u[0]), hi2(u[1]), hi2(u[2]), hi2(u[3]), hi2(u[4]), hi2(u[5]),
-                          hi2(u[6]), hi2(u[7]));
-      }
-      if (sa.nonfinite) ca = make_uint4(0u, 0u, 0u, 0u);
-      if (sb.nonfinite) cb = make_uint4(0u, 0u, 0u, 0u);
+      for (int g = 0; g < kWords; ++g) ca[g] = 0u;
+    }
+    if (sb.nonfinite) {
+#pragma unroll
+      for (int g = 0; g < kWords; ++g) cb[g] = 0u;
     }
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int c = 2 * p + half;
       const BlockScale& s = half ? sb : sa;
+      const uint32_t* cw = half ? cb : ca;
       const int64_t gcol = c0 + c;
-      if (gcol < cols && rows_ok)
-        *reinterpret_cast<uint4*>(args.q_col + gcol * (rows / 2) + (r0 + rb * 32) / 2) = half ? cb : ca;
+      if (gcol < cols && rows_ok) {
+        // codes of T^T: [cols, rows] bytes (MXFP8) or [cols, rows / 2] (MXFP4)
+        uint4* dst = reinterpret_cast<uint4*>(args.q_col + (gcol * rows + r0 + rb * 32) / (kFp8 ? 1 : 2));
+        dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        if constexpr (kFp8) dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+      }
       if (linear) {
         if (gcol < cols && rows_ok) args.sf_col[gcol * (rows / 32) + (r0 / 32) + rb] = (uint8_t)s.byte;
       } else {
@@ -486,17 +514,17 @@ __global__ void __launch_bounds__(kThreads, 3)
 
 namespace {
 
-template <bool kRow, bool kCol>
+template <bool kRow, bool kCol, bool kFp8 = false>
 cudaError_t launch_cast_t(const CUtensorMap& tm, const CastArgs& args, int col_tiles, int num_tiles,
                           int dev, cudaStream_t stream) {
   static std::atomic<int> ctas_per_sm[64];
   int per_sm = (dev >= 0 && dev < 64) ? ctas_per_sm[dev].load(std::memory_order_relaxed) : 0;
   if (per_sm == 0) {
-    cudaError_t e = cudaFuncSetAttribute(cast_kernel<kRow, kCol>,
+    cudaError_t e = cudaFuncSetAttribute(cast_kernel<kRow, kCol, kFp8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kCastSmemBytes);
     if (e != cudaSuccess) return e;
     int occ = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, cast_kernel<kRow, kCol>, kThreads,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, cast_kernel<kRow, kCol, kFp8>, kThreads,
                                                       kCastSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -513,7 +541,7 @@ cudaError_t launch_cast_t(const CUtensorMap& tm, const CastArgs& args, int col_t
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kCastSmemBytes;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, cast_kernel<kRow, kCol>, tm, args, col_tiles, num_tiles, status);
+  return cudaLaunchKernelEx(&cfg, cast_kernel<kRow, kCol, kFp8>, tm, args, col_tiles, num_tiles, status);
 }
 
 }  // namespace
@@ -539,6 +567,10 @@ cudaError_t launch_cast(const CastArgs& args, cudaStream_t stream) {
   if (col_tiles * row_tiles > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
   const int num_tiles = static_cast<int>(col_tiles * row_tiles);
   const bool row = args.q_row != nullptr, col = args.q_col != nullptr;
+  if (args.flags & kFlagFp8) {
+    if (row || !col) return cudaErrorInvalidValue;  // MXFP8: column output only
+    return launch_cast_t<false, true, true>(tm, args, int(col_tiles), num_tiles, dev, stream);
+  }
   if (row && col) return launch_cast_t<true, true>(tm, args, int(col_tiles), num_tiles, dev, stream);
   if (row) return launch_cast_t<true, false>(tm, args, int(col_tiles), num_tiles, dev, stream);
   if (col) return launch_cast_t<false, true>(tm, args, int(col_tiles), num_tiles, dev, stream);

@@ -57,14 +57,10 @@ namespace {
 constexpr int kBM = 256;                // rows of C per CTA pair
 constexpr int kRowsPerCta = 128;        // rows of A (and of B) held by each CTA
 constexpr int kBN = 256;                // columns of C per tile
-constexpr int kBK = 256;                // K elements per stage
-constexpr int kBKBytes = kBK / 2;       // 128 bytes = one swizzle row
+constexpr int kBKBytes = 128;           // code bytes per row per stage = one swizzle row
 constexpr int kStages = 6;
 constexpr int kAStage = kRowsPerCta * kBKBytes;  // 16 KiB
 constexpr int kBStage = kRowsPerCta * kBKBytes;  // 16 KiB
-constexpr int kSfaStage = 2 * 512;               // own 128-row tile x 2 K tiles
-constexpr int kSfbStage = 2 * 2 * 512;           // both 128-row tiles of B x 2 K tiles
-constexpr uint32_t kStageBytes = kAStage + kBStage + kSfaStage + kSfbStage;
 constexpr int kGroupM = 8;                        // raster group (pair row tiles)
 constexpr int kScaleWarps = 4;   // warps 2-5
 constexpr int kEpiWarps = 8;     // warps 6-13
@@ -73,25 +69,42 @@ constexpr int kThreads = 32 * (2 + kScaleWarps + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;
 constexpr uint32_t kSfCol0 = kBN;
-constexpr uint32_t kSfaCols = 8;                  // 2 K tiles x 4 columns
-constexpr uint32_t kSfStageCols = kSfaCols + 16;  // + 2 K tiles x 2 row tiles x 4 columns
-static_assert(kSfCol0 + kStages * kSfStageCols <= kTmemCols, "tensor memory budget");
-
-constexpr int kRingBytes = kStages * static_cast<int>(kStageBytes);
 constexpr int kOutStageBytes = 32 * 32 * 2;  // per epilogue warp: 32 rows x 32 bf16 columns
 constexpr int kBarrierBytes = (3 * kStages + 2) * 8 + 16;
 // The dynamic shared-memory window starts 1024-byte aligned in practice; the
 // spare bytes below cover a smaller alignment and the kernel checks it.
 constexpr int kSmemBytes = 232448;
-static_assert(kRingBytes + kEpiWarps * kOutStageBytes + kBarrierBytes <= kSmemBytes, "shared memory");
-constexpr uint32_t kSmemSlack = kSmemBytes - (kRingBytes + kEpiWarps * kOutStageBytes + kBarrierBytes);
 
-// Instruction descriptor, kind::mxf4: A and B E2M1 (format 1), both K-major,
-// fp32 accumulator, N >> 3 at bit 17, UE8M0 scales (bit 23), M >> 4 at bit
-// 24 (M = 256: the pair).  The scale-factor ids (bits 4-5 for B, 29-30 for A)
-// pick the byte pair of the 32-bit tensor-memory scale column an MMA reads.
-constexpr uint32_t kIdescBase = (1u << 7) | (1u << 10) | (uint32_t(kBN >> 3) << 17) | (1u << 23) |
-                                (uint32_t(kBM >> 4) << 24);
+// Operand element format.  MXFP4 (E2M1, two per byte): a 128-byte swizzle row
+// holds 256 K, consumed by four K = 64 kind::mxf4 MMAs, each reading a pair of
+// scale bytes (scale_vec::2X).  MXFP8 (E4M3, one per byte): 128 K per stage,
+// four K = 32 kind::mxf8f6f4 MMAs with one scale byte each (scale_vec::1X).
+// Scales come in 512-byte tiles of 128 rows x 4 K-blocks (128 K).
+template <bool kFp8>
+struct Fmt {
+  static constexpr int kBK = kFp8 ? 128 : 256;     // K elements per stage
+  static constexpr int kKTiles = kBK / 128;         // scale K-tiles per stage
+  static constexpr int kMmaK = kBK / 4;             // K per MMA
+  static constexpr int kMmasPerKTile = 4 / kKTiles;
+  static constexpr int kSfaStage = kKTiles * 512;        // own 128-row tile
+  static constexpr int kSfbStage = 2 * kKTiles * 512;    // both 128-row tiles of B
+  static constexpr uint32_t kStageBytes = kAStage + kBStage + kSfaStage + kSfbStage;
+  static constexpr uint32_t kSfaCols = kKTiles * 4;      // 4 tensor-memory columns per tile
+  static constexpr uint32_t kSfStageCols = kSfaCols + 2 * kKTiles * 4;
+  static constexpr int kRingBytes = kStages * static_cast<int>(kStageBytes);
+  static constexpr uint32_t kSmemSlack =
+      kSmemBytes - (kRingBytes + kEpiWarps * kOutStageBytes + kBarrierBytes);
+  // Instruction descriptor: A and B types (kind::mxf4: E2M1 = 1;
+  // kind::mxf8f6f4: E4M3 = 0) at bits 7 and 10, both K-major, fp32
+  // accumulator, N >> 3 at bit 17, UE8M0 scales (bit 23), M >> 4 at bit 24
+  // (M = 256: the pair).  The scale-factor ids (bits 4-5 for B, 29-30 for A)
+  // pick the byte(s) of the 32-bit tensor-memory scale column an MMA reads.
+  static constexpr uint32_t kIdescBase = (kFp8 ? 0u : ((1u << 7) | (1u << 10))) |
+                                         (uint32_t(kBN >> 3) << 17) | (1u << 23) |
+                                         (uint32_t(kBM >> 4) << 24);
+  static_assert(kSfCol0 + kStages * kSfStageCols <= kTmemCols, "tensor memory budget");
+  static_assert(kRingBytes + kEpiWarps * kOutStageBytes + kBarrierBytes <= kSmemBytes, "shared memory");
+};
 
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32) {
   uint32_t out;
@@ -118,12 +131,17 @@ struct PairGemmParams {
   int num_mt, num_nt, num_kt, ktiles128;
 };
 
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mxf4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSfa,
                           const __grid_constant__ CUtensorMap tmSfb,
                           const __grid_constant__ CUtensorMap tmC, const PairGemmParams p) {
+  using F = Fmt<kFp8>;
+  constexpr int kSfaStage = F::kSfaStage, kSfbStage = F::kSfbStage;
+  constexpr uint32_t kStageBytes = F::kStageBytes, kSfaCols = F::kSfaCols, kSfStageCols = F::kSfStageCols;
+  constexpr uint32_t kSmemSlack = F::kSmemSlack;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte-swizzled operand tiles (same offset
   // in both CTAs: identical kernels, identical static layout).
@@ -200,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const int kg0 = kt * 2;
+          const int kg0 = kt * F::kKTiles;
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
           tma_load_2d(sA + stage * kAStage, &tmA, &full[stage], kt * kBKBytes, a_row);
           tma_load_2d(sB + stage * kBStage, &tmB, &full[stage], kt * kBKBytes, b_row);
@@ -229,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t adesc0 = make_smem_desc(smem_u32(sA), 16, 1024, 2);
       const uint64_t bdesc0 = make_smem_desc(smem_u32(sB), 16, 1024, 2);
       // 64-deep k-steps of the last stage (K % 64 == 32 rounds up: zero codes).
-      const int last_nks =
-          static_cast<int>((args.K - static_cast<int64_t>(p.num_kt - 1) * kBK + 63) / 64);
+      const int last_nks = static_cast<int>(
+          (args.K - static_cast<int64_t>(p.num_kt - 1) * F::kBK + F::kMmaK - 1) / F::kMmaK);
       for (int t = pair; ok && t < num_tiles; t += num_pairs) {
         ok = mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, &g_device_status);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
@@ -252,10 +270,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               if (ks < nks) {
-                const uint32_t sf_id = (ks & 1) * 2;
-                tc_mma_pair_mxf4(tmem_base + kAccCol, a_d + 2 * ks, b_d + 2 * ks,
-                                 kIdescBase | (sf_id << 4) | (sf_id << 29), sf_col + (ks >> 1) * 4,
-                                 sf_col + kSfaCols + (ks >> 1) * 8, (kt | ks) != 0);
+                // K-tile g of the stage; byte (FP8) or byte pair (FP4) sf_id of its columns
+                const uint32_t g = ks / F::kMmasPerKTile;
+                const uint32_t sf_id = (ks % F::kMmasPerKTile) * (4 / F::kMmasPerKTile);
+                const uint32_t idesc = F::kIdescBase | (sf_id << 4) | (sf_id << 29);
+                if constexpr (kFp8)
+                  tc_mma_pair_mxf8f6f4(tmem_base + kAccCol, a_d + 2 * ks, b_d + 2 * ks, idesc,
+                                       sf_col + g * 4, sf_col + kSfaCols + g * 8, (kt | ks) != 0);
+                else
+                  tc_mma_pair_mxf4(tmem_base + kAccCol, a_d + 2 * ks, b_d + 2 * ks, idesc,
+                                   sf_col + g * 4, sf_col + kSfaCols + g * 8, (kt | ks) != 0);
               }
             }
             tc_commit_pair(&empty[stage], 0x3);
@@ -290,15 +314,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint8_t* sfa = sSfa + stage * kSfaStage + lane * 16;
-        const uint8_t* sfb = sSfb + stage * kSfbStage + lane * 16;
-        const uint4 a0 = lds128(sfa), a1 = lds128(sfa + 512);
-        const uint4 b00 = lds128(sfb), b10 = lds128(sfb + 1024);
-        const uint4 b01 = lds128(sfb + 512), b11 = lds128(sfb + 1536);
+        const uint8_t* sfb = sSfb + stage * kSfbStage + lane * 16;  // [row tile][K tile][512]
         const uint32_t taddr = tmem_base + lane_base + kSfCol0 + stage * kSfStageCols;
-        // columns 0-7: A, K tiles 0 and 1; 8-15: B K tile 0 (row tiles 0, 1); 16-23: B K tile 1
-        tmem_st_32x32b_x8(taddr + 0, a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w);
-        tmem_st_32x32b_x8(taddr + 8, b00.x, b00.y, b00.z, b00.w, b10.x, b10.y, b10.z, b10.w);
-        tmem_st_32x32b_x8(taddr + 16, b01.x, b01.y, b01.z, b01.w, b11.x, b11.y, b11.z, b11.w);
+        if constexpr (kFp8) {
+          // columns 0-3: A; 4-11: B (row tiles 0, 1), one K tile
+          const uint4 a0 = lds128(sfa), b0 = lds128(sfb), b1 = lds128(sfb + 512);
+          tmem_st_32x32b_x4(taddr + 0, a0.x, a0.y, a0.z, a0.w);
+          tmem_st_32x32b_x8(taddr + 4, b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w);
+        } else {
+          // columns 0-7: A, K tiles 0 and 1; 8-15: B K tile 0 (row tiles 0, 1); 16-23: B K tile 1
+          const uint4 a0 = lds128(sfa), a1 = lds128(sfa + 512);
+          const uint4 b00 = lds128(sfb), b10 = lds128(sfb + 1024);
+          const uint4 b01 = lds128(sfb + 512), b11 = lds128(sfb + 1536);
+          tmem_st_32x32b_x8(taddr + 0, a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w);
+          tmem_st_32x32b_x8(taddr + 8, b00.x, b00.y, b00.z, b00.w, b10.x, b10.y, b10.z, b10.w);
+          tmem_st_32x32b_x8(taddr + 16, b01.x, b01.y, b01.z, b01.w, b11.x, b11.y, b11.z, b11.w);
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -391,14 +422,15 @@ bool make_byte_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t 
 }
 
 // Scale tiles of an operand as a 3-D byte tensor [row tiles][K tiles x 4][128]
-// (each 512-byte tile is four 128-byte rows); boxes of 2 row tiles x 8 rows
-// (two K tiles) x 128 bytes, zero fill past the last row tile.
-bool make_scale_pair_map(CUtensorMap* map, const uint8_t* base, int64_t row_tiles, int64_t ktiles128) {
+// (each 512-byte tile is four 128-byte rows); boxes of 2 row tiles x
+// box_rows rows (box_rows / 4 K tiles) x 128 bytes, zero fill past the edges.
+bool make_scale_pair_map(CUtensorMap* map, const uint8_t* base, int64_t row_tiles, int64_t ktiles128,
+                         uint32_t box_rows) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(ktiles128 * 4), static_cast<cuuint64_t>(row_tiles)};
   cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(ktiles128 * 512)};
-  cuuint32_t box[3] = {128, 8, 2};
+  cuuint32_t box[3] = {128, box_rows, 2};
   cuuint32_t estrides[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base), dims, strides, box,
                   estrides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -422,16 +454,18 @@ bool make_bf16_out_map(CUtensorMap* map, uint16_t* base, int64_t M, int64_t N, i
 }
 
 // Shared-memory opt-in of the kernel, once per device.
+template <bool kFp8>
 cudaError_t prepare_kernel(int dev) {
   static std::atomic<bool> done[64];
   if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gemm_mxf4_pair_kernel,
+  cudaError_t e = cudaFuncSetAttribute(gemm_mxf4_pair_kernel<kFp8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
   return e;
 }
 
 // Largest number of co-resident CTA pairs, per device (cached).
+template <bool kFp8>
 int max_pairs(int dev) {
   static std::atomic<int> cache[64];
   if (dev >= 0 && dev < 64 && cache[dev].load(std::memory_order_relaxed) > 0)
@@ -448,7 +482,7 @@ int max_pairs(int dev) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_mxf4_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_mxf4_pair_kernel<kFp8>, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -506,33 +540,38 @@ cudaError_t launch_fill_zero_bf16(uint16_t* c, int64_t M, int64_t N, int64_t ldc
   return cudaLaunchKernelEx(&cfg, fill_zero_bf16_kernel, c, M, N, ldc);
 }
 
-cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream) {
+namespace {
+
+template <bool kFp8>
+cudaError_t launch_gemm_fmt(const GemmArgs& args, cudaStream_t stream) {
+  using F = Fmt<kFp8>;
   if (args.M == 0 || args.N == 0) return cudaSuccess;
   if (args.K == 0) return launch_fill_zero_bf16(args.c, args.M, args.N, args.ldc, stream);
   const int64_t ktiles128 = (args.K + 127) / 128;
   const int64_t a_sf_rows = (args.M + 127) / 128 * ktiles128 * 4;  // 128-byte rows of the scale buffer
+  const int64_t row_bytes = kFp8 ? args.K : args.K / 2;             // code bytes per row
 
   CUtensorMap tmA, tmB, tmSfa, tmSfb;
-  if (!make_byte_map(&tmA, args.a, args.M, args.K / 2, kBKBytes, kRowsPerCta, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_byte_map(&tmB, args.b, args.N, args.K / 2, kBKBytes, kRowsPerCta, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_byte_map(&tmSfa, args.a_sf, a_sf_rows, 128, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_scale_pair_map(&tmSfb, args.b_sf, (args.N + 127) / 128, ktiles128))
+  if (!make_byte_map(&tmA, args.a, args.M, row_bytes, kBKBytes, kRowsPerCta, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_byte_map(&tmB, args.b, args.N, row_bytes, kBKBytes, kRowsPerCta, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_byte_map(&tmSfa, args.a_sf, a_sf_rows, 128, 128, 4 * F::kKTiles, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_scale_pair_map(&tmSfb, args.b_sf, (args.N + 127) / 128, ktiles128, 4 * F::kKTiles))
     return cudaErrorInvalidValue;
   CUtensorMap tmC;
   if (!make_bf16_out_map(&tmC, args.c, args.M, args.N, args.ldc)) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = prepare_kernel(dev);
+  e = prepare_kernel<kFp8>(dev);
   if (e != cudaSuccess) return e;
   PairGemmParams p;
   p.args = args;
   p.num_mt = static_cast<int>((args.M + kBM - 1) / kBM);
   p.num_nt = static_cast<int>((args.N + kBN - 1) / kBN);
-  p.num_kt = static_cast<int>((args.K + kBK - 1) / kBK);
+  p.num_kt = static_cast<int>((args.K + F::kBK - 1) / F::kBK);
   p.ktiles128 = static_cast<int>(ktiles128);
   const int64_t tiles = static_cast<int64_t>(p.num_mt) * p.num_nt;
-  const int pairs = static_cast<int>(std::min<int64_t>(tiles, max_pairs(dev)));
+  const int pairs = static_cast<int>(std::min<int64_t>(tiles, max_pairs<kFp8>(dev)));
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
@@ -547,7 +586,15 @@ cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // the launch's own result (the thread's last error may be stale and unrelated)
-  return cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel, tmA, tmB, tmSfa, tmSfb, tmC, p);
+  return cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel<kFp8>, tmA, tmB, tmSfa, tmSfb, tmC, p);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream) { return launch_gemm_fmt<false>(args, stream); }
+
+cudaError_t launch_gemm_mxfp8(const GemmArgs& args, cudaStream_t stream) {
+  return launch_gemm_fmt<true>(args, stream);
 }
 
 }  // namespace mxfp4

@@ -10,6 +10,7 @@ namespace mxfp4 {
 constexpr uint32_t kFlagHadamardRow = 1u;
 constexpr uint32_t kFlagHadamardCol = 2u;
 constexpr uint32_t kFlagScaleLinear = 4u;
+constexpr uint32_t kFlagFp8 = 1u << 16;  // internal: E4M3 elements (column output only)
 
 struct CastArgs {
   const uint16_t* x;  // bf16 bits [rows, cols], pitch ldx
@@ -39,6 +40,8 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
+// The same GEMM on MXFP8 (E4M3) operands: codes [rows, K] bytes, same scale layout.
+cudaError_t launch_gemm_mxfp8(const GemmArgs& args, cudaStream_t stream);
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
 // (so the library needs no link-time dependency on libcuda); null if missing.

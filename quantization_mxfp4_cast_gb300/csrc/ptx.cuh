@@ -294,6 +294,20 @@ __device__ __forceinline__ void tc_cp_pair_32x128b_warpx4(uint32_t taddr, uint64
 
 // Pair MMA: D (128 rows in each CTA) (+)= A (128 rows in each CTA) . B^T with
 // B's N rows split half and half over the two CTAs' shared memory.
+// The FP8 form: kind::mxf8f6f4 with one UE8M0 scale per 32 K (scale_vec::1X),
+// K = 32 per instruction; the instruction descriptor gives the element types.
+__device__ __forceinline__ void tc_mma_pair_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                     uint32_t idesc, uint32_t sfa_tmem,
+                                                     uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
+      "}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_mma_pair_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                                  uint32_t idesc, uint32_t sfa_tmem,
                                                  uint32_t sfb_tmem, uint32_t accumulate) {
@@ -318,6 +332,13 @@ __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, uint32_t r0, u
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
       "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(r4), "r"(r5), "r"(r6), "r"(r7)
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t r0, uint32_t r1,
+                                                  uint32_t r2, uint32_t r3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r0),
+               "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_st_wait() {
