@@ -45,9 +45,6 @@ namespace {
 constexpr int kTile = 128;
 constexpr int kThreads = 256;
 
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
 // E2M1 codes of 8 values, element 0 in the low nibble of byte 0.  The
 // conversion rounds to nearest even and saturates at +-6.
 __device__ __forceinline__ uint32_t cvt8_e2m1(float v0, float v1, float v2, float v3, float v4,
@@ -98,12 +95,6 @@ __device__ __forceinline__ void block_codes(V v, uint32_t* out) {
 __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 

@@ -65,6 +65,20 @@ def test_gemm_fp4_random_codes_and_scales(m, M, N, K):
     assert_close(run_gemm_fp4(m, ca, sa, cb, sb, M, N, K), ref)
 
 
+@pytest.mark.parametrize("M,N,K", [(2336, 520, 14336), (8488, 264, 4096)])
+def test_gemm_fp4_partial_raster_group(m, M, N, K):
+    # The kernel walks the 256-row tiles in groups sized to K (8 row tiles at
+    # K = 14336, 32 at K = 4096); these shapes end in a partial group (10 =
+    # 8 + 2 and 34 = 32 + 2 row tiles) with a ragged last row and column tile.
+    rng = np.random.default_rng(M + N + K)
+    ca = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    cb = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sa = rng.integers(0x76, 0x7A, size=(M, K // 32), dtype=np.uint8)
+    sb = rng.integers(0x76, 0x7A, size=(N, K // 32), dtype=np.uint8)
+    ref = oracle.gemm_mxfp4(ca, sa, cb, sb, nthreads=8)
+    assert_close(run_gemm_fp4(m, ca, sa, cb, sb, M, N, K), ref, f"{M}x{N}x{K}")
+
+
 def test_gemm_fp4_one_hot_scales(m):
     # all codes 1.0; one scale byte raised per operand: isolates the scale
     # addressing (row, block) of both operands exactly
