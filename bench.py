@@ -351,6 +351,35 @@ def fp8_wgrad_leg(step, stream, iters=20):
                     "and the kind::mxf8f6f4 GEMM dW[N,K] = dY^T X"}
 
 
+def cast_out_leg(step, stream, iters=20):
+    """The dgrad GEMM with the next cast fused into its epilogue: dX = dY . W
+    written as bf16 and, by the same kernel, as MXFP4 (row-wise, and column-wise
+    with the Hadamard along M: the grad preset the layer below casts its
+    grad_out with), against the same GEMM followed by a separate dual cast
+    of dX.  Each variant timed on its own (CUDA events, back to back)."""
+    m = step.m
+    with torch.cuda.stream(stream):
+        dx = torch.empty(M, K, dtype=torch.bfloat16, device=step.x.device)
+        gemm = lambda: m.gemm_fp4(step.qdy[0], step.qdy[1], step.qw[2], step.qw[3], M, K, N, c=dx,
+                                  stream=stream)
+        gemm()
+        qdx = m.mxfp4_cast_dual(dx, hadamard_col=True, stream=stream)
+        cast = lambda: m.mxfp4_cast_dual(dx, hadamard_col=True, out=qdx, stream=stream)
+        fused = lambda: m.gemm_fp4_cast_out(step.qdy[0], step.qdy[1], step.qw[2], step.qw[3], M, K, N,
+                                            hadamard_col=True, c=dx, out=qdx, stream=stream)
+        t_gemm = time_loop(gemm, iters, 3, stream)
+        t_cast = time_loop(cast, iters, 3, stream)
+        t_sep = time_loop(lambda: (gemm(), cast()), iters, 3, stream)
+        t_fused = time_loop(fused, iters, 3, stream)
+    flop = 2.0 * M * N * K
+    return {"unit": "us", "dgrad_us": t_gemm * 1e6, "dual_cast_dx_us": t_cast * 1e6,
+            "dgrad_then_cast_us": t_sep * 1e6, "dgrad_cast_out_us": t_fused * 1e6,
+            "saved_us": (t_sep - t_fused) * 1e6,
+            "dgrad_cast_out_tflops": flop / t_fused / 1e12,
+            "what": "dX[8192,14336] = dY . W (MXFP4) plus the dual MXFP4 cast of dX (row; column with "
+                    "Hadamard): separate cast kernel vs the cast written by the GEMM's epilogue"}
+
+
 def fp8_reference_leg(dev, stream, iters=20):
     """cuBLASLt FP8 (e4m3, per-tensor scales, bf16 out) through torch._scaled_mm
     on the step's three GEMM shapes, operands pre-quantized: context for the
@@ -641,6 +670,7 @@ def main():
         extra["layer"] = layer_leg(step, stream)
         extra["mxfp8_wgrad"] = fp8_wgrad_leg(step, stream)
         extra["fp8_cublaslt_reference"] = fp8_reference_leg(dev, stream)
+        extra["dgrad_cast_out"] = cast_out_leg(step, stream)
         if m.device_status() != 0:
             raise RuntimeError("device status word set in the layer leg")
 

@@ -136,6 +136,29 @@ mxfp4_status gemm_fp4(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, c
                       uint16_t* c, int64_t M, int64_t N, int64_t K, int64_t ldc, void* stream);
 
 /*
+ * gemm_fp4_cast_out -- gemm_fp4 whose epilogue also casts its own output to
+ * MXFP4, so the next GEMM's operand comes without a separate cast of C (the
+ * gradient one GEMM produces is the next one's grad_out: jax-aiter README,
+ * "MXFP4 training architecture"; the pages run the casts as separate calls).
+ *   a .. ldc     : as gemm_fp4 (C is always written)
+ *   q_row/sf_row : C quantized along N: codes [M, N/2], tile scales (M rows,
+ *                  N/32 blocks) -- what mxfp4_cast_dual writes as its row
+ *                  output for x = C; both NULL to skip
+ *   q_col/sf_col : C^T quantized along M: codes [N, M/2], tile scales (N rows,
+ *                  M/32 blocks) -- mxfp4_cast_dual's column output; both NULL
+ *                  to skip
+ *   flags        : MXFP4_HADAMARD_ROW, MXFP4_HADAMARD_COL (tile layout only)
+ * The cast outputs are bit-identical to mxfp4_cast_dual(C, flags) on the bf16
+ * C this call writes, scale padding (0x00) included.  Requires M % 32 == 0,
+ * N % 32 == 0, K % 32 == 0; M*N == 0 is a no-op; K == 0 writes zeros and the
+ * casts of a zero matrix.
+ */
+mxfp4_status gemm_fp4_cast_out(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
+                               const uint8_t* b_sf, uint16_t* c, int64_t M, int64_t N, int64_t K,
+                               int64_t ldc, uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col,
+                               uint8_t* sf_col, uint32_t flags, void* stream);
+
+/*
  * MXFP8: the FP8 alternative for the wgrad operands (jax-aiter README,
  * "MXFP4 training architecture": an FP8 dB path next to the FP4 one).
  * E4M3 elements (one byte each, round to nearest even, saturating at 448)

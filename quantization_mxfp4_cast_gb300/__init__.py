@@ -35,7 +35,7 @@ ABI_SYMBOLS = (
     "mxfp4_cast", "mxfp4_cast_dual", "gemm_fp4", "mxfp4_workspace_bytes",
     "gemm_fp4_bf16_fwd", "gemm_fp4_bf16_dgrad", "gemm_fp4_bf16_wgrad", "mxfp4_device_status",
     "gemm_fp4_bf16_fwd_noalloc", "mxfp4_last_cuda_error", "mxfp4_cuda_error_string",
-    "mxfp8_cast_cols", "gemm_mxfp8", "gemm_fp8_bf16_wgrad",
+    "mxfp8_cast_cols", "gemm_mxfp8", "gemm_fp8_bf16_wgrad", "gemm_fp4_cast_out",
 )
 
 _lib = None
@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
                 "gemm_mxfp8": (I, [P, P, P, P, P, I64, I64, I64, I64, P]),
                 "gemm_fp8_bf16_wgrad": (I, [P, P, P, I64, I64, I64, U32, P, SZ, P]),
                 "mxfp4_cuda_error_string": (ctypes.c_char_p, [I]),
+                "gemm_fp4_cast_out": (I, [P, P, P, P, P, I64, I64, I64, I64, P, P, P, P, U32, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -183,6 +184,30 @@ def gemm_fp4(a, a_sf, b, b_sf, M: int, N: int, K: int, c=None, stream=None):
     _check(lib().gemm_fp4(_ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), _ptr(c), M, N, K, c.stride(0),
                           _stream(stream)), "gemm_fp4")
     return c
+
+
+def gemm_fp4_cast_out(a, a_sf, b, b_sf, M: int, N: int, K: int, row=True, col=True,
+                      hadamard_row=False, hadamard_col=False, c=None, out=None, stream=None):
+    """C[M,N] (bf16) = A . B^T like gemm_fp4, plus the MXFP4 casts of C written by
+    the GEMM's epilogue: row-wise (C along N) and/or column-wise (C^T along M),
+    the same bytes as mxfp4_cast_dual(C).  M, N, K multiples of 32.
+    Returns (c, q_row, sf_row, q_col, sf_col); skipped outputs are None.
+    `out` = (q_row, sf_row, q_col, sf_col) reuses buffers (None entries skip)."""
+    _need_cuda(a, a_sf, b, b_sf)
+    dev = a.device
+    if c is None:
+        c = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    if out is None:
+        u8 = lambda n: torch.empty(n, dtype=torch.uint8, device=dev)
+        out = ((u8(M * N // 2).view(M, N // 2), u8(scales_bytes(M, N))) if row else (None, None)) + \
+              ((u8(N * M // 2).view(N, M // 2), u8(scales_bytes(N, M))) if col else (None, None))
+    q_row, sf_row, q_col, sf_col = out
+    flags = (MXFP4_HADAMARD_ROW if hadamard_row else 0) | (MXFP4_HADAMARD_COL if hadamard_col else 0)
+    _check(lib().gemm_fp4_cast_out(_ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), _ptr(c), M, N, K, c.stride(0),
+                                   _ptr(q_row), _ptr(sf_row), _ptr(q_col), _ptr(sf_col), flags,
+                                   _stream(stream)),
+           "gemm_fp4_cast_out")
+    return c, q_row, sf_row, q_col, sf_col
 
 
 def _workspace(op, M, N, K, ws, device):

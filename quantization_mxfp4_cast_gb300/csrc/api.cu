@@ -251,6 +251,42 @@ mxfp4_status gemm_mxfp8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
   return gemm_checked(a, a_sf, b, b_sf, c, M, N, K, ldc, static_cast<cudaStream_t>(stream), true);
 }
 
+mxfp4_status gemm_fp4_cast_out(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
+                               const uint8_t* b_sf, uint16_t* c, int64_t M, int64_t N, int64_t K,
+                               int64_t ldc, uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col,
+                               uint8_t* sf_col, uint32_t flags, void* stream) {
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return MXFP4_ERR_INVALID_ARG;
+  if (K % 32 != 0 || M % 32 != 0 || N % 32 != 0 || ldc < N) return MXFP4_ERR_INVALID_ARG;
+  if (flags & ~(MXFP4_HADAMARD_ROW | MXFP4_HADAMARD_COL)) return MXFP4_ERR_INVALID_ARG;
+  if ((q_row == nullptr) != (sf_row == nullptr) || (q_col == nullptr) != (sf_col == nullptr))
+    return MXFP4_ERR_INVALID_ARG;
+  if (ceil_div(M, 128) > 65535) return MXFP4_ERR_INVALID_ARG;  // the K == 0 path casts C
+  if (M == 0 || N == 0) return MXFP4_OK;
+  MXFP4_TRY(check_out(c));
+  if (ldc % 8 != 0) return MXFP4_ERR_MISALIGNED;
+  if (q_row != nullptr) {
+    MXFP4_TRY(check_out(q_row));
+    MXFP4_TRY(check_out(sf_row));
+  }
+  if (q_col != nullptr) {
+    MXFP4_TRY(check_out(q_col));
+    MXFP4_TRY(check_out(sf_col));
+  }
+  if (K > 0) {
+    MXFP4_TRY(check_out(a));
+    MXFP4_TRY(check_out(a_sf));
+    MXFP4_TRY(check_out(b));
+    MXFP4_TRY(check_out(b_sf));
+  }
+  MXFP4_TRY(check_device(c));
+  const GemmArgs g{a, a_sf, b, b_sf, c, M, N, K, ldc};
+  const mxfp4::CastOutArgs out{q_row, sf_row, q_col, sf_col, flags};
+  const cudaError_t e = mxfp4::launch_gemm_cast_out(g, out, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidValue) return MXFP4_ERR_INVALID_ARG;
+  return from_cuda(e);
+}
+
 mxfp4_status mxfp8_cast_cols(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
                              uint8_t* q_col, uint8_t* sf_col, uint32_t flags, void* stream) {
   if (flags & ~(MXFP4_HADAMARD_COL | MXFP4_SCALE_LINEAR)) return MXFP4_ERR_INVALID_ARG;

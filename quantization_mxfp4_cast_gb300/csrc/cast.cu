@@ -38,28 +38,13 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace mxfp4 {
 namespace {
 
 constexpr int kTile = 128;
 constexpr int kThreads = 256;
-
-// E2M1 codes of 8 values, element 0 in the low nibble of byte 0.  The
-// conversion rounds to nearest even and saturates at +-6.
-__device__ __forceinline__ uint32_t cvt8_e2m1(float v0, float v1, float v2, float v3, float v4,
-                                              float v5, float v6, float v7) {
-  uint32_t out;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
-      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
-      : "=r"(out)
-      : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
-  return out;
-}
 
 // E4M3 codes of 4 values, element 0 in the low byte.  The conversion rounds
 // to nearest even and saturates at +-448 (cvt puts its first source in the
@@ -120,41 +105,6 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   return r;
 }
 
-// From the largest magnitude's bit pattern: scale byte and the exact
-// power-of-two multiplier 2^-e (as fp32, and as a bf16 bit pattern).  For a
-// finite amax with biased exponent E, floor(log2 amax) - kEmax + 127 =
-// E - kEmax, clamped at 0 (E = 0 covers zero and subnormals); kEmax is the
-// exponent of the element format's largest value (E2M1: 6 = 1.5 * 2^2 -> 2;
-// E4M3: 448 = 1.75 * 2^8 -> 8).
-struct BlockScale {
-  uint32_t byte;
-  float mult;
-  uint32_t mult_bf16;
-  bool nonfinite;
-};
-
-template <int kEmax = 2>
-__device__ __forceinline__ BlockScale block_scale(uint32_t amax_bits) {
-  BlockScale s;
-  s.nonfinite = amax_bits >= 0x7F800000u;
-  const int e_biased = static_cast<int>(amax_bits >> 23);
-  const int byte = e_biased > kEmax ? e_biased - kEmax : 0;
-  s.mult = __uint_as_float(static_cast<uint32_t>(254 - byte) << 23);
-  s.mult_bf16 = static_cast<uint32_t>(254 - byte) << 7;
-  s.byte = s.nonfinite ? 0xFFu : static_cast<uint32_t>(byte);
-  return s;
-}
-
-// Codes of 8 fp32 elements under the block's scale (the conversion keeps the
-// sign of values that round to zero, so no fix-up is needed).
-__device__ __forceinline__ uint32_t quantize8(const float* y, const BlockScale& s) {
-  if (s.nonfinite) return 0u;
-  const float m = s.mult;
-  return cvt8_e2m1(__fmul_rn(y[0], m), __fmul_rn(y[1], m), __fmul_rn(y[2], m),
-                   __fmul_rn(y[3], m), __fmul_rn(y[4], m), __fmul_rn(y[5], m),
-                   __fmul_rn(y[6], m), __fmul_rn(y[7], m));
-}
-
 // fp32 value of the bf16 element in the low (kHi = false) or high half of w,
 // times s (a bf16 bit pattern), by the mixed-precision fma with -0 added:
 // for a power-of-two s the product is exact in fp32 down to 2^-126 (anything
@@ -182,17 +132,7 @@ __device__ __forceinline__ uint32_t quantize8_bf16(uint32_t w0, uint32_t w1, uin
                    bf16_times<false>(w3, s), bf16_times<true>(w3, s));
 }
 
-// fp32 value nearest to 1/sqrt(32).
-constexpr float kInvSqrt32 = 0x1.6a09e6p-3f;  // bit pattern 0x3E3504F3
-
 __device__ __forceinline__ int sf_in_tile(int r, int b) { return (r & 31) * 16 + (r >> 5) * 4 + b; }
-
-// max(|a|, |b|, |c|) with NaN propagation (three-input form).
-__device__ __forceinline__ float max3_nan_abs(float a, float b, float c) {
-  float r;
-  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)), "f"(fabsf(c)));
-  return r;
-}
 
 // Packed bf16 magnitude max of 2^n words as a balanced tree (independent
 // operations instead of one serial chain).  Sign bits of the result are
@@ -208,22 +148,6 @@ __device__ __forceinline__ uint32_t tree_absmax_bf16x2(const uint32_t* w) {
     for (int i = 0; i < n; ++i) m[i] = absmax_bf16x2(m[2 * i], m[2 * i + 1]);
   }
   return m[0];
-}
-
-// NaN-propagating max |v| of 32 fp32 values read as v(i), i = 0..31, in four
-// independent chains of three-input maxima.
-template <typename F>
-__device__ __forceinline__ float amax32(F v) {
-  float c[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int b = 8 * k;
-    float m = max3_nan_abs(v(b), v(b + 1), v(b + 2));
-    m = max3_nan_abs(m, v(b + 3), v(b + 4));
-    m = max3_nan_abs(m, v(b + 5), v(b + 6));
-    c[k] = max3_nan_abs(m, v(b + 7), 0.f);
-  }
-  return max3_nan_abs(c[0], c[1], max3_nan_abs(c[2], c[3], 0.f));
 }
 
 // A 128 x 128 bf16 tile in shared memory is two 128-row halves of 64 columns

@@ -44,11 +44,26 @@
 //     whole-line and asynchronous while the next tile's MMAs run.
 // M and N tails come from the TMA out-of-bounds zero fill on loads and the
 // TMA clipping of stores; a K tail (K % 64 == 32) reads zero codes past K.
+//
+// Output cast (the kCastOut instance): the epilogue also writes C as MXFP4,
+// row-wise (C quantized along N) and column-wise (C^T quantized along M),
+// each optional, with the optional Hadamard per output -- the same bytes a
+// separate dual cast of the bf16 C would write, without reading C back
+// (jax-aiter README, "MXFP4 training architecture": the gradient that one
+// GEMM produces is cast for the next).  Each epilogue lane holds one row of
+// its 128 columns, so the row blocks are quantized from registers; the column
+// blocks are read back, one column per lane, from the 32 x 32 bf16 blocks the
+// epilogue already stages in shared memory for the C store.  Codes leave
+// through two more TMA stores per warp and tile, scales as direct stores.
+// Rows past M and columns past N hold exact zeros (zero-filled operands), so
+// the scale padding comes out 0x00 as the cast writes it.  The two code
+// staging buffers take the room of one ring stage (5 stages instead of 6).
 #include <algorithm>
 #include <atomic>
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace mxfp4 {
 
@@ -62,7 +77,6 @@ constexpr int kBM = 256;                // rows of C per CTA pair
 constexpr int kRowsPerCta = 128;        // rows of A (and of B) held by each CTA
 constexpr int kBN = 256;                // columns of C per tile
 constexpr int kBKBytes = 128;           // code bytes per row per stage = one swizzle row
-constexpr int kStages = 6;
 constexpr int kAStage = kRowsPerCta * kBKBytes;  // 16 KiB
 constexpr int kBStage = kRowsPerCta * kBKBytes;  // 16 KiB
 constexpr int64_t kRasterPanelBytes = int64_t(24) << 20;  // A panel of one raster group
@@ -74,7 +88,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;
 constexpr uint32_t kSfCol0 = kBN;
 constexpr int kOutStageBytes = 32 * 32 * 2;  // per epilogue warp: 32 rows x 32 bf16 columns
-constexpr int kBarrierBytes = (3 * kStages + 2) * 8 + 16;
 // The dynamic shared-memory window starts 1024-byte aligned in practice; the
 // spare bytes below cover a smaller alignment and the kernel checks it.
 constexpr int kSmemBytes = 232448;
@@ -84,8 +97,10 @@ constexpr int kSmemBytes = 232448;
 // scale bytes (scale_vec::2X).  MXFP8 (E4M3, one per byte): 128 K per stage,
 // four K = 32 kind::mxf8f6f4 MMAs with one scale byte each (scale_vec::1X).
 // Scales come in 512-byte tiles of 128 rows x 4 K-blocks (128 K).
-template <bool kFp8>
+template <bool kFp8, bool kCastOut = false>
 struct Fmt {
+  static_assert(!(kFp8 && kCastOut), "the output cast is MXFP4 only");
+  static constexpr int kStages = kCastOut ? 5 : 6;
   static constexpr int kBK = kFp8 ? 128 : 256;     // K elements per stage
   static constexpr int kKTiles = kBK / 128;         // scale K-tiles per stage
   static constexpr int kMmaK = kBK / 4;             // K per MMA
@@ -96,8 +111,10 @@ struct Fmt {
   static constexpr uint32_t kSfaCols = kKTiles * 4;      // 4 tensor-memory columns per tile
   static constexpr uint32_t kSfStageCols = kSfaCols + 2 * kKTiles * 4;
   static constexpr int kRingBytes = kStages * static_cast<int>(kStageBytes);
-  static constexpr uint32_t kSmemSlack =
-      kSmemBytes - (kRingBytes + kEpiWarps * kOutStageBytes + kBarrierBytes);
+  // epilogue staging per warp: the bf16 C block, plus row and column codes
+  static constexpr int kEpiBytes = kEpiWarps * kOutStageBytes * (kCastOut ? 3 : 1);
+  static constexpr int kBarrierBytes = (3 * kStages + 2) * 8 + 16;
+  static constexpr uint32_t kSmemSlack = kSmemBytes - (kRingBytes + kEpiBytes + kBarrierBytes);
   // Instruction descriptor: A and B types (kind::mxf4: E2M1 = 1;
   // kind::mxf8f6f4: E4M3 = 0) at bits 7 and 10, both K-major, fp32
   // accumulator, N >> 3 at bit 17, UE8M0 scales (bit 23), M >> 4 at bit 24
@@ -107,7 +124,7 @@ struct Fmt {
                                          (uint32_t(kBN >> 3) << 17) | (1u << 23) |
                                          (uint32_t(kBM >> 4) << 24);
   static_assert(kSfCol0 + kStages * kSfStageCols <= kTmemCols, "tensor memory budget");
-  static_assert(kRingBytes + kEpiWarps * kOutStageBytes + kBarrierBytes <= kSmemBytes, "shared memory");
+  static_assert(kRingBytes + kEpiBytes + kBarrierBytes <= kSmemBytes, "shared memory");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32) {
@@ -135,16 +152,27 @@ struct PairGemmParams {
   GemmArgs args;
   int num_mt, num_nt, num_kt, ktiles128;
   int group_m;  // raster group, in pair row tiles
+  // output cast (kCastOut instance): tile-layout scales of C along N and of
+  // C^T along M (each null when that output is not wanted), Hadamard flags,
+  // and the scale tile counts ceil(M / 128), ceil(N / 128)
+  uint8_t* sf_row;
+  uint8_t* sf_col;
+  uint32_t cast_flags;
+  int m_tiles128, n_tiles128;
 };
 
-template <bool kFp8>
+template <bool kFp8, bool kCastOut>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mxf4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmSfa,
                           const __grid_constant__ CUtensorMap tmSfb,
-                          const __grid_constant__ CUtensorMap tmC, const PairGemmParams p) {
-  using F = Fmt<kFp8>;
+                          const __grid_constant__ CUtensorMap tmC,
+                          const __grid_constant__ CUtensorMap tmQr,  // row codes of C (kCastOut)
+                          const __grid_constant__ CUtensorMap tmQc,  // column codes of C (kCastOut)
+                          const PairGemmParams p) {
+  using F = Fmt<kFp8, kCastOut>;
+  constexpr int kStages = F::kStages;
   constexpr int kSfaStage = F::kSfaStage, kSfbStage = F::kSfbStage;
   constexpr uint32_t kStageBytes = F::kStageBytes, kSfaCols = F::kSfaCols, kSfStageCols = F::kSfStageCols;
   constexpr uint32_t kSmemSlack = F::kSmemSlack;
@@ -163,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sSfa = sB + kStages * kBStage;
   uint8_t* sSfb = sSfa + kStages * kSfaStage;
   uint8_t* sOut = sSfb + kStages * kSfbStage;  // epilogue staging, 1024-byte aligned
-  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + kEpiWarps * kOutStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + F::kEpiBytes);
   uint64_t* empty = full + kStages;
   uint64_t* sf_ready = empty + kStages;
   uint64_t* acc_full = sf_ready + kStages;
@@ -195,6 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmSfa);
     tma_prefetch_desc(&tmSfb);
     tma_prefetch_desc(&tmC);
+    if constexpr (kCastOut) {
+      if (p.sf_row != nullptr) tma_prefetch_desc(&tmQr);
+      if (p.sf_col != nullptr) tma_prefetch_desc(&tmQc);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, kTmemCols);
@@ -351,7 +383,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                         // tensor-memory lane quarter this warp may read
     const int h = (warp - kFirstEpiWarp) >> 2;      // which 128-column half of the tile
     const uint32_t acc_empty_leader = map_to_cta(acc_empty, 0);
-    const uint32_t out_buf = smem_u32(sOut + (warp - kFirstEpiWarp) * kOutStageBytes);
+    const int ew = warp - kFirstEpiWarp;
+    const uint32_t out_buf = smem_u32(sOut + ew * kOutStageBytes);
+    // output cast: row-code block (32 rows x 64 bytes, 64-byte swizzle like
+    // the C block) and column codes (128 column rows x 16 bytes)
+    const uint32_t rq_buf = smem_u32(sOut + (kEpiWarps + ew) * kOutStageBytes);
+    const uint32_t cq_buf = smem_u32(sOut + (2 * kEpiWarps + ew) * kOutStageBytes);
+    const bool do_row = kCastOut && p.sf_row != nullptr;
+    const bool do_col = kCastOut && p.sf_col != nullptr;
+    const bool had_row = (p.cast_flags & kFlagHadamardRow) != 0;
+    const bool had_col = (p.cast_flags & kFlagHadamardCol) != 0;
     uint32_t acc_phase = 0;
     for (int t = pair; t < num_tiles; t += num_pairs) {
       int mt, nt;
@@ -362,6 +403,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + h * 128;
       const int32_t row0 = mt * kBM + static_cast<int32_t>(rank) * kRowsPerCta + q * 32;
       const int32_t col0 = nt * kBN + h * 128;
+      // output cast: this warp's 32 rows and 128 columns sit in one 128-row
+      // scale tile of each output (row tile mt * 2 + rank, column tile
+      // nt * 2 + h); tiles past the padded extent are not written
+      const int rt128 = mt * 2 + static_cast<int>(rank), ct128 = nt * 2 + h;
+      const bool sf_tiles_ok = kCastOut && rt128 < p.m_tiles128 && ct128 < p.n_tiles128;
+      const size_t row_sf_tile = (static_cast<size_t>(rt128) * p.n_tiles128 + ct128) * 512;
+      const size_t col_sf_tile = (static_cast<size_t>(ct128) * p.m_tiles128 + rt128) * 512;
+      uint32_t row_sf = 0;
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -387,9 +436,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tmC, sOut + (warp - kFirstEpiWarp) * kOutStageBytes, col0 + c * 32, row0);
+          tma_store_2d(&tmC, sOut + ew * kOutStageBytes, col0 + c * 32, row0);
           bulk_commit_group();
         }
+        if constexpr (kCastOut) {
+          if (do_row) {  // block c of this lane's row, read back from the staged block
+            // (from shared memory rather than the packed registers: the cast then
+            // cannot be scheduled ahead of the accumulator release, and pk dies
+            // with the block stores -- measured 7-14% faster, no spills)
+            float y[32];
+            uint32_t q4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 w = lds128(sOut + ew * kOutStageBytes + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4));
+              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                y[8 * j + 2 * i] = __uint_as_float(ww[i] << 16);
+                y[8 * j + 2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
+              }
+            }
+            const BlockScale s = quantize_block32(y, had_row, q4);
+            row_sf |= s.byte << (8 * c);
+            sts128(rq_buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), q4[0], q4[1], q4[2], q4[3]);
+          }
+          if (do_col) {  // column c * 32 + lane of the staged block: 32 rows
+            float y[32];
+            uint32_t q4[4];
+            const uint32_t cb = out_buf + (lane & 7) * 2;
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+              y[r] = __uint_as_float(lds_u16(cb + r * 64 + (((lane >> 3) ^ ((r >> 1) & 3)) << 4)) << 16);
+            const BlockScale s = quantize_block32(y, had_col, q4);
+            sts128(cq_buf + (c * 32 + lane) * 16, q4[0], q4[1], q4[2], q4[3]);
+            if (sf_tiles_ok) p.sf_col[col_sf_tile + lane * 16 + c * 4 + q] = static_cast<uint8_t>(s.byte);
+          }
+        }
+      }
+      if constexpr (kCastOut) {
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0 && (do_row || do_col)) {
+          if (do_row) tma_store_2d(&tmQr, sOut + (kEpiWarps + ew) * kOutStageBytes, col0 / 2, row0);
+          if (do_col) tma_store_2d(&tmQc, sOut + (2 * kEpiWarps + ew) * kOutStageBytes, row0 / 2, col0);
+          bulk_commit_group();
+        }
+        // scales of this lane's row: blocks 0-3 of the 128-column tile, one word
+        if (do_row && sf_tiles_ok)
+          *reinterpret_cast<uint32_t*>(p.sf_row + row_sf_tile + lane * 16 + q * 4) = row_sf;
       }
       acc_phase ^= 1u;
     }
@@ -460,18 +554,18 @@ bool make_bf16_out_map(CUtensorMap* map, uint16_t* base, int64_t M, int64_t N, i
 }
 
 // Shared-memory opt-in of the kernel, once per device.
-template <bool kFp8>
+template <bool kFp8, bool kCastOut>
 cudaError_t prepare_kernel(int dev) {
   static std::atomic<bool> done[64];
   if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gemm_mxf4_pair_kernel<kFp8>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_mxf4_pair_kernel<kFp8, kCastOut>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
   return e;
 }
 
 // Largest number of co-resident CTA pairs, per device (cached).
-template <bool kFp8>
+template <bool kFp8, bool kCastOut>
 int max_pairs(int dev) {
   static std::atomic<int> cache[64];
   if (dev >= 0 && dev < 64 && cache[dev].load(std::memory_order_relaxed) > 0)
@@ -488,7 +582,8 @@ int max_pairs(int dev) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_mxf4_pair_kernel<kFp8>, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_mxf4_pair_kernel<kFp8, kCastOut>, &cfg) != cudaSuccess ||
+      n <= 0) {
     cudaGetLastError();
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -548,11 +643,17 @@ cudaError_t launch_fill_zero_bf16(uint16_t* c, int64_t M, int64_t N, int64_t ldc
 
 namespace {
 
-template <bool kFp8>
-cudaError_t launch_gemm_fmt(const GemmArgs& args, cudaStream_t stream) {
-  using F = Fmt<kFp8>;
+template <bool kFp8, bool kCastOut = false>
+cudaError_t launch_gemm_fmt(const GemmArgs& args, cudaStream_t stream, const CastOutArgs* out = nullptr) {
+  using F = Fmt<kFp8, kCastOut>;
   if (args.M == 0 || args.N == 0) return cudaSuccess;
-  if (args.K == 0) return launch_fill_zero_bf16(args.c, args.M, args.N, args.ldc, stream);
+  if (args.K == 0) {  // C = 0, and its casts are those of a zero matrix
+    cudaError_t e = launch_fill_zero_bf16(args.c, args.M, args.N, args.ldc, stream);
+    if (e != cudaSuccess || !kCastOut || (out->sf_row == nullptr && out->sf_col == nullptr)) return e;
+    const CastArgs ca{args.c, args.M, args.N, args.ldc, out->q_row, out->sf_row, out->q_col, out->sf_col,
+                      out->flags};
+    return launch_cast(ca, stream);
+  }
   const int64_t ktiles128 = (args.K + 127) / 128;
   const int64_t a_sf_rows = (args.M + 127) / 128 * ktiles128 * 4;  // 128-byte rows of the scale buffer
   const int64_t row_bytes = kFp8 ? args.K : args.K / 2;             // code bytes per row
@@ -565,10 +666,19 @@ cudaError_t launch_gemm_fmt(const GemmArgs& args, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   CUtensorMap tmC;
   if (!make_bf16_out_map(&tmC, args.c, args.M, args.N, args.ldc)) return cudaErrorInvalidValue;
+  // output cast: row codes [M, N/2] in 32-row x 64-byte boxes (64-byte
+  // swizzle), column codes [N, M/2] in 128-row x 16-byte boxes
+  CUtensorMap tmQr = {}, tmQc = {};
+  if (kCastOut && out->q_row != nullptr &&
+      !make_byte_map(&tmQr, out->q_row, args.M, args.N / 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  if (kCastOut && out->q_col != nullptr &&
+      !make_byte_map(&tmQc, out->q_col, args.N, args.M / 2, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = prepare_kernel<kFp8>(dev);
+  e = prepare_kernel<kFp8, kCastOut>(dev);
   if (e != cudaSuccess) return e;
   PairGemmParams p;
   p.args = args;
@@ -578,8 +688,13 @@ cudaError_t launch_gemm_fmt(const GemmArgs& args, cudaStream_t stream) {
   p.ktiles128 = static_cast<int>(ktiles128);
   p.group_m = 1;  // powers of two up to 64 while the A panel stays within the budget
   while (p.group_m < 64 && 2 * p.group_m * kBM * row_bytes <= kRasterPanelBytes) p.group_m *= 2;
+  p.sf_row = kCastOut ? out->sf_row : nullptr;
+  p.sf_col = kCastOut ? out->sf_col : nullptr;
+  p.cast_flags = kCastOut ? out->flags : 0u;
+  p.m_tiles128 = static_cast<int>((args.M + 127) / 128);
+  p.n_tiles128 = static_cast<int>((args.N + 127) / 128);
   const int64_t tiles = static_cast<int64_t>(p.num_mt) * p.num_nt;
-  const int pairs = static_cast<int>(std::min<int64_t>(tiles, max_pairs<kFp8>(dev)));
+  const int pairs = static_cast<int>(std::min<int64_t>(tiles, max_pairs<kFp8, kCastOut>(dev)));
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
@@ -594,7 +709,8 @@ cudaError_t launch_gemm_fmt(const GemmArgs& args, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // the launch's own result (the thread's last error may be stale and unrelated)
-  return cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel<kFp8>, tmA, tmB, tmSfa, tmSfb, tmC, p);
+  return cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel<kFp8, kCastOut>, tmA, tmB, tmSfa, tmSfb, tmC, tmQr,
+                            tmQc, p);
 }
 
 }  // namespace
@@ -603,6 +719,10 @@ cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream) { return laun
 
 cudaError_t launch_gemm_mxfp8(const GemmArgs& args, cudaStream_t stream) {
   return launch_gemm_fmt<true>(args, stream);
+}
+
+cudaError_t launch_gemm_cast_out(const GemmArgs& args, const CastOutArgs& out, cudaStream_t stream) {
+  return launch_gemm_fmt<false, true>(args, stream, &out);
 }
 
 }  // namespace mxfp4

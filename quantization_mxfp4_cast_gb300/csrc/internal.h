@@ -40,6 +40,17 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
+
+// The MXFP4 dual cast of the GEMM's own bf16 output, written by its epilogue.
+struct CastOutArgs {
+  uint8_t* q_row;   // codes [M, N/2] of C quantized along N, or null
+  uint8_t* sf_row;  // its tile-layout scales (null iff q_row is)
+  uint8_t* q_col;   // codes [N, M/2] of C^T quantized along M, or null
+  uint8_t* sf_col;  // its tile-layout scales (null iff q_col is)
+  uint32_t flags;   // kFlagHadamardRow, kFlagHadamardCol
+};
+// Requires M % 32 == 0 and N % 32 == 0.
+cudaError_t launch_gemm_cast_out(const GemmArgs& args, const CastOutArgs& out, cudaStream_t stream);
 // The same GEMM on MXFP8 (E4M3) operands: codes [rows, K] bytes, same scale layout.
 cudaError_t launch_gemm_mxfp8(const GemmArgs& args, cudaStream_t stream);
 
