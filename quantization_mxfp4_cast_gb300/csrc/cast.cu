@@ -75,80 +75,7 @@ __device__ __forceinline__ void block_codes(V v, uint32_t* out) {
   }
 }
 
-// Elementwise max(|a|, |b|) of bf16 pairs, NaN-propagating (sign bits of
-// the result are the XOR of the inputs' and must be masked off).
-__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-// Packed fp32 pairs (Blackwell f32x2 arithmetic, IEEE round-to-nearest per lane).
-__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
-  return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
-}
-__device__ __forceinline__ float lo2(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
-__device__ __forceinline__ float hi2(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-
-// fp32 value of the bf16 element in the low (kHi = false) or high half of w,
-// times s (a bf16 bit pattern), by the mixed-precision fma with -0 added:
-// for a power-of-two s the product is exact in fp32 down to 2^-126 (anything
-// smaller has |v| < 1/4 and gives a signed zero code either way), and adding
-// -0 keeps the sign of a zero product.  With s = 1 this is the plain widening.
-template <bool kHi>
-__device__ __forceinline__ float bf16_times(uint32_t w, uint16_t s) {
-  float r;
-  if constexpr (kHi)
-    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tfma.rn.f32.bf16 %0, h, %2, 0f80000000;\n\t}"
-        : "=f"(r) : "r"(w), "h"(s));
-  else
-    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tfma.rn.f32.bf16 %0, l, %2, 0f80000000;\n\t}"
-        : "=f"(r) : "r"(w), "h"(s));
-  return r;
-}
-constexpr uint16_t kBf16One = 0x3F80;
-
-// Codes of the 8 bf16 elements in 4 packed words (element 2i in the low half
-// of word i), scaled by the power of two s (bf16 bit pattern).
-__device__ __forceinline__ uint32_t quantize8_bf16(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
-                                                   uint16_t s) {
-  return cvt8_e2m1(bf16_times<false>(w0, s), bf16_times<true>(w0, s), bf16_times<false>(w1, s),
-                   bf16_times<true>(w1, s), bf16_times<false>(w2, s), bf16_times<true>(w2, s),
-                   bf16_times<false>(w3, s), bf16_times<true>(w3, s));
-}
-
 __device__ __forceinline__ int sf_in_tile(int r, int b) { return (r & 31) * 16 + (r >> 5) * 4 + b; }
-
-// Packed bf16 magnitude max of 2^n words as a balanced tree (independent
-// operations instead of one serial chain).  Sign bits of the result are
-// meaningless.
-template <int kN>
-__device__ __forceinline__ uint32_t tree_absmax_bf16x2(const uint32_t* w) {
-  uint32_t m[kN / 2];
-#pragma unroll
-  for (int i = 0; i < kN / 2; ++i) m[i] = absmax_bf16x2(w[2 * i], w[2 * i + 1]);
-#pragma unroll
-  for (int n = kN / 4; n >= 1; n >>= 1) {
-#pragma unroll
-    for (int i = 0; i < n; ++i) m[i] = absmax_bf16x2(m[2 * i], m[2 * i + 1]);
-  }
-  return m[0];
-}
 
 // A 128 x 128 bf16 tile in shared memory is two 128-row halves of 64 columns
 // (128 bytes per row), each written by one TMA load with the 128-byte

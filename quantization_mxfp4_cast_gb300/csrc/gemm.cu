@@ -444,30 +444,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (from shared memory rather than the packed registers: the cast then
             // cannot be scheduled ahead of the accumulator release, and pk dies
             // with the block stores -- measured 7-14% faster, no spills)
-            float y[32];
-            uint32_t q4[4];
+            uint32_t w[16], q4[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const uint4 w = lds128(sOut + ew * kOutStageBytes + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4));
-              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                y[8 * j + 2 * i] = __uint_as_float(ww[i] << 16);
-                y[8 * j + 2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
-              }
+              const uint4 v = lds128(sOut + ew * kOutStageBytes + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4));
+              w[4 * j] = v.x;
+              w[4 * j + 1] = v.y;
+              w[4 * j + 2] = v.z;
+              w[4 * j + 3] = v.w;
             }
-            const BlockScale s = quantize_block32(y, had_row, q4);
+            BlockScale s;
+            if (!had_row) {
+              s = quantize_bf16_block(w, q4);
+            } else {
+              float y[32];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                y[2 * i] = __uint_as_float(w[i] << 16);
+                y[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+              }
+              s = quantize_hadamard_block(y, q4);
+            }
             row_sf |= s.byte << (8 * c);
             sts128(rq_buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), q4[0], q4[1], q4[2], q4[3]);
           }
           if (do_col) {  // column c * 32 + lane of the staged block: 32 rows
-            float y[32];
             uint32_t q4[4];
             const uint32_t cb = out_buf + (lane & 7) * 2;
+            auto elem = [&](int r) { return lds_u16(cb + r * 64 + (((lane >> 3) ^ ((r >> 1) & 3)) << 4)); };
+            BlockScale s;
+            if (!had_col) {
+              uint32_t w[16];  // rows 2i, 2i + 1 as one bf16 pair
 #pragma unroll
-            for (int r = 0; r < 32; ++r)
-              y[r] = __uint_as_float(lds_u16(cb + r * 64 + (((lane >> 3) ^ ((r >> 1) & 3)) << 4)) << 16);
-            const BlockScale s = quantize_block32(y, had_col, q4);
+              for (int i = 0; i < 16; ++i) w[i] = __byte_perm(elem(2 * i), elem(2 * i + 1), 0x5410);
+              s = quantize_bf16_block(w, q4);
+            } else {
+              float y[32];
+#pragma unroll
+              for (int r = 0; r < 32; ++r) y[r] = __uint_as_float(elem(r) << 16);
+              s = quantize_hadamard_block(y, q4);
+            }
             sts128(cq_buf + (c * 32 + lane) * 16, q4[0], q4[1], q4[2], q4[3]);
             if (sf_tiles_ok) p.sf_col[col_sf_tile + lane * 16 + c * 4 + q] = static_cast<uint8_t>(s.byte);
           }
