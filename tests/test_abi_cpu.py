@@ -106,6 +106,15 @@ def test_argument_validation_before_any_launch(L):
     assert L.gemm_fp4_bf16_dgrad(good, good, good, 64, 48, 64, good, 1 << 30, None) == INV
     assert L.gemm_fp4_bf16_wgrad(good, good, good, 48, 64, 64, 0, good, 1 << 30, None) == INV
     assert L.gemm_fp4_bf16_wgrad(good, good, good, 64, 64, 64, 1, good, 1 << 30, None) == INV
+    # GEMM with the output cast: M and N multiples of 32, tile-layout flags
+    # only, codes and scales given together, aligned outputs, empty no-op
+    co = L.gemm_fp4_cast_out
+    assert co(good, good, good, good, good, 48, 64, 64, 64, good, good, good, good, 0, None) == INV
+    assert co(good, good, good, good, good, 64, 48, 64, 48, good, good, good, good, 0, None) == INV
+    assert co(good, good, good, good, good, 64, 64, 64, 64, good, good, good, good, 4, None) == INV
+    assert co(good, good, good, good, good, 64, 64, 64, 64, good, None, good, good, 0, None) == INV
+    assert co(good, good, good, good, good, 64, 64, 64, 64, good, good, odd, good, 0, None) == MIS
+    assert co(None, None, None, None, None, 0, 64, 64, 64, None, None, None, None, 2, None) == 0
     st = ctypes.c_int(0)
     assert L.mxfp4_device_status(0, None) == INV
 
