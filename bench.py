@@ -380,6 +380,77 @@ def cast_out_leg(step, stream, iters=20):
                     "Hadamard): separate cast kernel vs the cast written by the GEMM's epilogue"}
 
 
+def time_each(fn, iters, stream, flush):
+    """Mean seconds of fn() launched alone on `stream`, L2 overwritten before
+    each launch (the flush sits outside the timed events)."""
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for e0, e1 in evs:
+            flush.fill_(1.0)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    return sum(e0.elapsed_time(e1) for e0, e1 in evs) / iters / 1e3
+
+
+def cast_only_leg(m, dev, stream, hbm_gbs, iters=10):
+    """The cast-only workload: bf16 activations [8192, 4096] ~ N(0,1) with 0.1%
+    of the entries scaled by 50; the dual cast (row-wise + transposed) with
+    the Hadamard off and on (both outputs), and the row-wise cast alone."""
+    x = synth.cast_input().to(dev)
+    R, C = x.shape
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    dual = m.mxfp4_cast_dual(x, stream=stream)
+    row = m.mxfp4_cast(x, stream=stream)
+    runs = {
+        "dual": (lambda: m.mxfp4_cast_dual(x, out=dual, stream=stream), 3.0625),
+        "dual_hadamard_row_col": (lambda: m.mxfp4_cast_dual(x, hadamard_row=True, hadamard_col=True, out=dual,
+                                                             stream=stream), 3.0625),
+        "row_only": (lambda: m.mxfp4_cast(x, q=row[0], sf=row[1], stream=stream), 2.53125),
+    }
+    out = {}
+    for name, (fn, bpe) in runs.items():
+        t = time_each(fn, iters, stream, flush)
+        gbs = R * C * bpe / t / 1e9
+        out[name] = {"us": t * 1e6, "gbs": gbs, "frac_of_measured_hbm": gbs / hbm_gbs, "frac_of_8tbs": gbs / 8000.0}
+    del flush
+    return {"shape": [R, C], "bytes_per_element": {"dual": 3.0625, "row_only": 2.53125}, **out,
+            "what": "cast-only workload (activations with 0.1% outliers x50), each launch alone after an "
+                    "L2 overwrite, CUDA events"}
+
+
+def gemm_shapes_leg(m, dev, stream, iters=10):
+    """Per-GEMM throughput at the Llama shapes: the 8B gate/up forward and the
+    fwd / dgrad / wgrad of every 70B layer, on pre-quantized operands (random
+    codes, scales 2^-9 .. 2^-6: the time does not depend on the values)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    rnd = lambda n: torch.randint(0, 256, (n,), dtype=torch.uint8, device=dev, generator=g)
+    sf = lambda r, k: torch.randint(0x76, 0x7A, (m.scales_bytes(r, k),), dtype=torch.uint8, device=dev,
+                                    generator=g)
+    cases = [("llama8b_gate_up", "fwd")] + [(n, d) for n in ("llama70b_qkv", "llama70b_o", "llama70b_gate_up",
+                                                              "llama70b_down") for d in ("fwd", "dgrad", "wgrad")]
+    out, flop_total, time_total = {}, 0.0, 0.0
+    for name, which in cases:
+        M_, N_, K_, _ = synth.LLAMA_SHAPES[name]
+        mo, no, kc = {"fwd": (M_, N_, K_), "dgrad": (M_, K_, N_), "wgrad": (N_, K_, M_)}[which]
+        a, b = rnd(mo * kc // 2), rnd(no * kc // 2)
+        a_sf, b_sf = sf(mo, kc), sf(no, kc)
+        c = torch.empty(mo, no, dtype=torch.bfloat16, device=dev)
+        t = time_loop(lambda: m.gemm_fp4(a, a_sf, b, b_sf, mo, no, kc, c=c, stream=stream), iters, 3, stream)
+        flop = 2.0 * mo * no * kc
+        out[f"{name}.{which}"] = {"M": mo, "N": no, "K": kc, "tflops": flop / t / 1e12, "us": t * 1e6}
+        flop_total += flop
+        time_total += t
+        del a, b, a_sf, b_sf, c
+    return {"unit": "TFLOP/s", "gemms": out, "flop_weighted_tflops": flop_total / time_total / 1e12,
+            "what": "gemm_fp4 at the 8B gate/up forward and the 70B layer shapes (M = 8192 tokens), "
+                    "CUDA events, back to back"}
+
+
 def fp8_reference_leg(dev, stream, iters=20):
     """cuBLASLt FP8 (e4m3, per-tensor scales, bf16 out) through torch._scaled_mm
     on the step's three GEMM shapes, operands pre-quantized: context for the
@@ -671,6 +742,8 @@ def main():
         extra["mxfp8_wgrad"] = fp8_wgrad_leg(step, stream)
         extra["fp8_cublaslt_reference"] = fp8_reference_leg(dev, stream)
         extra["dgrad_cast_out"] = cast_out_leg(step, stream)
+        extra["cast_only"] = cast_only_leg(m, dev, stream, peaks["hbm"])
+        extra["gemm_shapes"] = gemm_shapes_leg(m, dev, stream)
         if m.device_status() != 0:
             raise RuntimeError("device status word set in the layer leg")
 
