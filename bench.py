@@ -451,6 +451,47 @@ def gemm_shapes_leg(m, dev, stream, iters=10):
                     "CUDA events, back to back"}
 
 
+def stack_leg(dev, stream, iters=10):
+    """Two layers back to back at the 8B MLP shapes (up: 4096 -> 14336, then
+    down: 14336 -> 4096; nothing between them), forward + backward with the
+    weights' casts cached: MXFP4LinearStack (each GEMM casts its output for
+    the next one in its epilogue, no bf16 intermediate) against a chain of
+    two MXFP4Linear layers (bf16 intermediates, separate casts)."""
+    from quantization_mxfp4_cast_gb300.layer import MXFP4Linear, MXFP4LinearStack
+    w_up = synth.normal_bf16((K, N), 0.02, seed=71).to(dev)
+    w_down = synth.normal_bf16((N, K), 0.02, seed=72).to(dev)
+    x = synth.normal_bf16((M, N), 1.0, seed=73).to(dev)
+    dy = synth.normal_bf16((M, N), 1e-3, seed=74).to(dev)
+    with torch.cuda.stream(stream):
+        stack = MXFP4LinearStack([w_up.clone(), w_down.clone()])
+        chain = [MXFP4Linear(w_up.clone(), cache_name="up"), MXFP4Linear(w_down.clone(), cache_name="down")]
+        xs = x.clone().requires_grad_(True)
+        xc = x.clone().requires_grad_(True)
+
+        def run_stack():
+            stack(xs).backward(dy)
+            xs.grad = None
+            for p in stack.weights:
+                p.grad = None
+
+        def run_chain():
+            h = xc
+            for layer in chain:
+                h = layer(h)
+            h.backward(dy)
+            xc.grad = None
+            for layer in chain:
+                layer.weight.grad = None
+
+        t_stack = time_loop(run_stack, iters, 3, stream)
+        t_chain = time_loop(run_chain, iters, 3, stream)
+    flop = 2 * 3 * 2.0 * M * N * K
+    return {"unit": "TFLOP/s", "stack_tflops": flop / t_stack / 1e12, "chain_tflops": flop / t_chain / 1e12,
+            "stack_ms": t_stack * 1e3, "chain_ms": t_chain * 1e3, "saved_us": (t_chain - t_stack) * 1e6,
+            "what": "x[8192,4096] -> up W[14336,4096] -> down W[4096,14336], fwd + bwd (6 GEMMs): "
+                    "MXFP4LinearStack (casts fused into the producing GEMMs) vs two MXFP4Linear layers"}
+
+
 def fp8_reference_leg(dev, stream, iters=20):
     """cuBLASLt FP8 (e4m3, per-tensor scales, bf16 out) through torch._scaled_mm
     on the step's three GEMM shapes, operands pre-quantized: context for the
@@ -744,6 +785,7 @@ def main():
         extra["dgrad_cast_out"] = cast_out_leg(step, stream)
         extra["cast_only"] = cast_only_leg(m, dev, stream, peaks["hbm"])
         extra["gemm_shapes"] = gemm_shapes_leg(m, dev, stream)
+        extra["stack"] = stack_leg(dev, stream)
         if m.device_status() != 0:
             raise RuntimeError("device status word set in the layer leg")
 

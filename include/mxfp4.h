@@ -140,7 +140,8 @@ mxfp4_status gemm_fp4(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, c
  * MXFP4, so the next GEMM's operand comes without a separate cast of C (the
  * gradient one GEMM produces is the next one's grad_out: jax-aiter README,
  * "MXFP4 training architecture"; the pages run the casts as separate calls).
- *   a .. ldc     : as gemm_fp4 (C is always written)
+ *   a .. ldc     : as gemm_fp4; c may be NULL (then no bf16 C is written and
+ *                  ldc is ignored) when at least one cast output is given
  *   q_row/sf_row : C quantized along N: codes [M, N/2], tile scales (M rows,
  *                  N/32 blocks) -- what mxfp4_cast_dual writes as its row
  *                  output for x = C; both NULL to skip
@@ -149,9 +150,9 @@ mxfp4_status gemm_fp4(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, c
  *                  to skip
  *   flags        : MXFP4_HADAMARD_ROW, MXFP4_HADAMARD_COL (tile layout only)
  * The cast outputs are bit-identical to mxfp4_cast_dual(C, flags) on the bf16
- * C this call writes, scale padding (0x00) included.  Requires M % 32 == 0,
- * N % 32 == 0, K % 32 == 0; M*N == 0 is a no-op; K == 0 writes zeros and the
- * casts of a zero matrix.
+ * C (whether or not it is stored), scale padding (0x00) included.  Requires
+ * M % 32 == 0, N % 32 == 0, K % 32 == 0; M*N == 0 is a no-op; K == 0 writes
+ * zeros and the casts of a zero matrix (all bytes 0x00).
  */
 mxfp4_status gemm_fp4_cast_out(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
                                const uint8_t* b_sf, uint16_t* c, int64_t M, int64_t N, int64_t K,

@@ -187,15 +187,18 @@ def gemm_fp4(a, a_sf, b, b_sf, M: int, N: int, K: int, c=None, stream=None):
 
 
 def gemm_fp4_cast_out(a, a_sf, b, b_sf, M: int, N: int, K: int, row=True, col=True,
-                      hadamard_row=False, hadamard_col=False, c=None, out=None, stream=None):
+                      hadamard_row=False, hadamard_col=False, c=None, out=None, write_c=True, stream=None):
     """C[M,N] (bf16) = A . B^T like gemm_fp4, plus the MXFP4 casts of C written by
     the GEMM's epilogue: row-wise (C along N) and/or column-wise (C^T along M),
     the same bytes as mxfp4_cast_dual(C).  M, N, K multiples of 32.
     Returns (c, q_row, sf_row, q_col, sf_col); skipped outputs are None.
-    `out` = (q_row, sf_row, q_col, sf_col) reuses buffers (None entries skip)."""
+    `out` = (q_row, sf_row, q_col, sf_col) reuses buffers (None entries skip).
+    write_c=False stores no bf16 C (c comes back None): only the casts."""
     _need_cuda(a, a_sf, b, b_sf)
     dev = a.device
-    if c is None:
+    if not write_c:
+        c = None
+    elif c is None:
         c = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     if out is None:
         u8 = lambda n: torch.empty(n, dtype=torch.uint8, device=dev)
@@ -203,7 +206,8 @@ def gemm_fp4_cast_out(a, a_sf, b, b_sf, M: int, N: int, K: int, row=True, col=Tr
               ((u8(N * M // 2).view(N, M // 2), u8(scales_bytes(N, M))) if col else (None, None))
     q_row, sf_row, q_col, sf_col = out
     flags = (MXFP4_HADAMARD_ROW if hadamard_row else 0) | (MXFP4_HADAMARD_COL if hadamard_col else 0)
-    _check(lib().gemm_fp4_cast_out(_ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), _ptr(c), M, N, K, c.stride(0),
+    ldc = c.stride(0) if c is not None else N
+    _check(lib().gemm_fp4_cast_out(_ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), _ptr(c), M, N, K, ldc,
                                    _ptr(q_row), _ptr(sf_row), _ptr(q_col), _ptr(sf_col), flags,
                                    _stream(stream)),
            "gemm_fp4_cast_out")

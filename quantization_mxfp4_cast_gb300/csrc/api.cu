@@ -257,14 +257,17 @@ mxfp4_status gemm_fp4_cast_out(const uint8_t* a, const uint8_t* a_sf, const uint
                                uint8_t* sf_col, uint32_t flags, void* stream) {
   if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
     return MXFP4_ERR_INVALID_ARG;
-  if (K % 32 != 0 || M % 32 != 0 || N % 32 != 0 || ldc < N) return MXFP4_ERR_INVALID_ARG;
+  if (K % 32 != 0 || M % 32 != 0 || N % 32 != 0) return MXFP4_ERR_INVALID_ARG;
   if (flags & ~(MXFP4_HADAMARD_ROW | MXFP4_HADAMARD_COL)) return MXFP4_ERR_INVALID_ARG;
   if ((q_row == nullptr) != (sf_row == nullptr) || (q_col == nullptr) != (sf_col == nullptr))
     return MXFP4_ERR_INVALID_ARG;
-  if (ceil_div(M, 128) > 65535) return MXFP4_ERR_INVALID_ARG;  // the K == 0 path casts C
+  if (c != nullptr && ldc < N) return MXFP4_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return MXFP4_OK;
-  MXFP4_TRY(check_out(c));
-  if (ldc % 8 != 0) return MXFP4_ERR_MISALIGNED;
+  if (c == nullptr && q_row == nullptr && q_col == nullptr) return MXFP4_ERR_INVALID_ARG;  // no output
+  if (c != nullptr) {
+    MXFP4_TRY(check_out(c));
+    if (ldc % 8 != 0) return MXFP4_ERR_MISALIGNED;
+  }
   if (q_row != nullptr) {
     MXFP4_TRY(check_out(q_row));
     MXFP4_TRY(check_out(sf_row));
@@ -279,7 +282,8 @@ mxfp4_status gemm_fp4_cast_out(const uint8_t* a, const uint8_t* a_sf, const uint
     MXFP4_TRY(check_out(b));
     MXFP4_TRY(check_out(b_sf));
   }
-  MXFP4_TRY(check_device(c));
+  MXFP4_TRY(check_device(c != nullptr ? static_cast<const void*>(c)
+                                       : (q_row != nullptr ? static_cast<const void*>(q_row) : q_col)));
   const GemmArgs g{a, a_sf, b, b_sf, c, M, N, K, ldc};
   const mxfp4::CastOutArgs out{q_row, sf_row, q_col, sf_col, flags};
   const cudaError_t e = mxfp4::launch_gemm_cast_out(g, out, static_cast<cudaStream_t>(stream));

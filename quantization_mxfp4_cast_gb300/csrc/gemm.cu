@@ -436,7 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tmC, sOut + ew * kOutStageBytes, col0 + c * 32, row0);
+          if (!kCastOut || p.args.c != nullptr)  // the cast-only form writes no bf16 C
+            tma_store_2d(&tmC, sOut + ew * kOutStageBytes, col0 + c * 32, row0);
           bulk_commit_group();
         }
         if constexpr (kCastOut) {
@@ -663,12 +664,17 @@ template <bool kFp8, bool kCastOut = false>
 cudaError_t launch_gemm_fmt(const GemmArgs& args, cudaStream_t stream, const CastOutArgs* out = nullptr) {
   using F = Fmt<kFp8, kCastOut>;
   if (args.M == 0 || args.N == 0) return cudaSuccess;
-  if (args.K == 0) {  // C = 0, and its casts are those of a zero matrix
-    cudaError_t e = launch_fill_zero_bf16(args.c, args.M, args.N, args.ldc, stream);
-    if (e != cudaSuccess || !kCastOut || (out->sf_row == nullptr && out->sf_col == nullptr)) return e;
-    const CastArgs ca{args.c, args.M, args.N, args.ldc, out->q_row, out->sf_row, out->q_col, out->sf_col,
-                      out->flags};
-    return launch_cast(ca, stream);
+  if (args.K == 0) {  // C = 0, and its casts are those of a zero matrix: all bytes 0x00
+    cudaError_t e = args.c != nullptr ? launch_fill_zero_bf16(args.c, args.M, args.N, args.ldc, stream)
+                                      : cudaSuccess;
+    if (e != cudaSuccess || !kCastOut) return e;
+    const size_t code_bytes = static_cast<size_t>(args.M) * static_cast<size_t>(args.N / 2);
+    const size_t sf_bytes = static_cast<size_t>((args.M + 127) / 128) * ((args.N + 127) / 128) * 512;
+    if (out->q_row != nullptr && e == cudaSuccess) e = cudaMemsetAsync(out->q_row, 0, code_bytes, stream);
+    if (out->sf_row != nullptr && e == cudaSuccess) e = cudaMemsetAsync(out->sf_row, 0, sf_bytes, stream);
+    if (out->q_col != nullptr && e == cudaSuccess) e = cudaMemsetAsync(out->q_col, 0, code_bytes, stream);
+    if (out->sf_col != nullptr && e == cudaSuccess) e = cudaMemsetAsync(out->sf_col, 0, sf_bytes, stream);
+    return e;
   }
   const int64_t ktiles128 = (args.K + 127) / 128;
   const int64_t a_sf_rows = (args.M + 127) / 128 * ktiles128 * 4;  // 128-byte rows of the scale buffer
@@ -680,8 +686,9 @@ cudaError_t launch_gemm_fmt(const GemmArgs& args, cudaStream_t stream, const Cas
       !make_byte_map(&tmSfa, args.a_sf, a_sf_rows, 128, 128, 4 * F::kKTiles, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_scale_pair_map(&tmSfb, args.b_sf, (args.N + 127) / 128, ktiles128, 4 * F::kKTiles))
     return cudaErrorInvalidValue;
-  CUtensorMap tmC;
-  if (!make_bf16_out_map(&tmC, args.c, args.M, args.N, args.ldc)) return cudaErrorInvalidValue;
+  CUtensorMap tmC = {};
+  if (args.c != nullptr && !make_bf16_out_map(&tmC, args.c, args.M, args.N, args.ldc))
+    return cudaErrorInvalidValue;
   // output cast: row codes [M, N/2] in 32-row x 64-byte boxes (64-byte
   // swizzle), column codes [N, M/2] in 128-row x 16-byte boxes
   CUtensorMap tmQr = {}, tmQc = {};

@@ -49,7 +49,8 @@ struct CastOutArgs {
   uint8_t* sf_col;  // its tile-layout scales (null iff q_col is)
   uint32_t flags;   // kFlagHadamardRow, kFlagHadamardCol
 };
-// Requires M % 32 == 0 and N % 32 == 0.
+// Requires M % 32 == 0 and N % 32 == 0.  args.c may be null (no bf16 C is
+// written) when at least one cast output is given.
 cudaError_t launch_gemm_cast_out(const GemmArgs& args, const CastOutArgs& out, cudaStream_t stream);
 // The same GEMM on MXFP8 (E4M3) operands: codes [rows, K] bytes, same scale layout.
 cudaError_t launch_gemm_mxfp8(const GemmArgs& args, cudaStream_t stream);

@@ -17,6 +17,7 @@ CUDA kernels through the binding, on the current torch stream.
     ws = WeightWorkspace()
     w_q = ws.get_or_quantize(w, q, cache_name="mlp_down")   # recast only when w changed
     y = MXFP4Linear(w, cache_name="mlp_down")(x)             # autograd: fwd, dgrad, wgrad
+    y = MXFP4LinearStack([w1, w2])(x)       # layers back to back, casts fused into the GEMMs
 """
 from __future__ import annotations
 
@@ -24,7 +25,7 @@ from dataclasses import dataclass
 
 import torch
 
-from . import gemm_fp4, mxfp4_cast_dual, scales_bytes
+from . import gemm_fp4, gemm_fp4_cast_out, mxfp4_cast_dual, scales_bytes
 
 
 @dataclass
@@ -177,3 +178,92 @@ class MXFP4Linear(torch.nn.Module):
 
     def forward(self, x: torch.Tensor) -> torch.Tensor:
         return mxfp4_linear(x, self.weight, workspace=self.workspace, cache_name=self.cache_name)
+
+
+class _MXFP4StackFn(torch.autograd.Function):
+    """y = x W_0^T W_1^T ... W_{L-1}^T, layers back to back with nothing in
+    between, every GEMM in MXFP4.  Each forward GEMM but the last writes, in
+    its epilogue, the next layer's activation casts instead of a bf16 output;
+    each dgrad but the first writes the casts of dX that the layer below takes
+    as its grad_out.  So the only separate casts are those of the input and of
+    the incoming gradient, and the numbers are those of a chain of
+    MXFP4Linear layers: a fused cast equals the separate cast of the bf16
+    tensor it replaces, byte for byte.  The saved activations are their
+    quantized copies (what wgrad reads), not bf16 tensors."""
+
+    @staticmethod
+    def forward(ctx, x2, w_qs, *ws):
+        M = x2.shape[0]
+        stream = torch.cuda.current_stream(x2.device)
+        x_q = MXFP4Quantizer.for_activation().quantize(x2)
+        acts, y = [], None
+        for i, (w, w_q) in enumerate(zip(ws, w_qs)):
+            N, K = w.shape
+            acts.append(x_q)
+            if i + 1 < len(ws):
+                nxt = MXFP4Tensor.empty(M, N, True, x2.device)
+                gemm_fp4_cast_out(x_q.q_row, x_q.sf_row, w_q.q_row, w_q.sf_row, M, N, K, hadamard_col=True,
+                                  out=(nxt.q_row, nxt.sf_row, nxt.q_col, nxt.sf_col), write_c=False,
+                                  stream=stream)
+                x_q = nxt
+            else:
+                y = gemm_fp4(x_q.q_row, x_q.sf_row, w_q.q_row, w_q.sf_row, M, N, K, stream=stream)
+        ctx.acts, ctx.w_qs, ctx.shapes, ctx.M = acts, w_qs, [tuple(w.shape) for w in ws], M
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        M, L = ctx.M, len(ctx.w_qs)
+        stream = torch.cuda.current_stream(dy.device)
+        dy_q = MXFP4Quantizer.for_grad().quantize(dy.contiguous())
+        dws, dx = [None] * L, None
+        for i in reversed(range(L)):
+            N, K = ctx.shapes[i]
+            x_q, w_q = ctx.acts[i], ctx.w_qs[i]
+            if ctx.needs_input_grad[2 + i]:
+                # dW_i[N,K] = dY_i^T . X_i, contraction over the tokens
+                dws[i] = gemm_fp4(dy_q.q_col, dy_q.sf_col, x_q.q_col, x_q.sf_col, N, K, M, stream=stream)
+            if i > 0:
+                # dX_i = dY_i . W_i is the grad_out of layer i-1: only its casts
+                nxt = MXFP4Tensor.empty(M, K, True, dy.device)
+                gemm_fp4_cast_out(dy_q.q_row, dy_q.sf_row, w_q.q_col, w_q.sf_col, M, K, N, hadamard_col=True,
+                                  out=(nxt.q_row, nxt.sf_row, nxt.q_col, nxt.sf_col), write_c=False,
+                                  stream=stream)
+                dy_q = nxt
+            elif ctx.needs_input_grad[0]:
+                dx = gemm_fp4(dy_q.q_row, dy_q.sf_row, w_q.q_col, w_q.sf_col, M, K, N, stream=stream)
+        return (dx, None, *dws)
+
+
+class MXFP4LinearStack(torch.nn.Module):
+    """Bias-free linear layers applied back to back (weights W_i[N_i, K_i] with
+    K_{i+1} = N_i, nothing between them) whose training step runs in MXFP4,
+    each GEMM handing the next one its operand already quantized.  The
+    weights' casts are cached in `workspace` like MXFP4Linear's.  Every
+    dimension, and the number of tokens, must be a multiple of 32."""
+
+    def __init__(self, weights, cache_prefix: str = "stack", workspace: WeightWorkspace | None = None):
+        super().__init__()
+        if len(weights) == 0:
+            raise ValueError("MXFP4LinearStack needs at least one weight")
+        for i, w in enumerate(weights):
+            if w.dim() != 2 or w.shape[0] % 32 or w.shape[1] % 32:
+                raise ValueError(f"weight {i}: expected [N, K] with N, K multiples of 32, got {tuple(w.shape)}")
+            if i and w.shape[1] != weights[i - 1].shape[0]:
+                raise ValueError(f"weight {i} takes {w.shape[1]} inputs, weight {i - 1} gives {weights[i - 1].shape[0]}")
+        self.weights = torch.nn.ParameterList([torch.nn.Parameter(w) for w in weights])
+        self.cache_prefix = cache_prefix
+        self.workspace = workspace if workspace is not None else WeightWorkspace()
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        if x.dtype != torch.bfloat16:
+            raise ValueError("MXFP4LinearStack expects bf16 input")
+        x2 = x.reshape(-1, x.shape[-1])
+        if not x2.is_contiguous():
+            x2 = x2.contiguous()
+        if x2.shape[0] % 32:
+            raise ValueError("the number of tokens must be a multiple of 32")
+        wq = MXFP4Quantizer.for_weight()
+        w_qs = [self.workspace.get_or_quantize(w, wq, f"{self.cache_prefix}.{i}") for i, w in enumerate(self.weights)]
+        y = _MXFP4StackFn.apply(x2, w_qs, *self.weights)
+        return y.reshape(*x.shape[:-1], y.shape[-1])

@@ -115,6 +115,9 @@ def test_argument_validation_before_any_launch(L):
     assert co(good, good, good, good, good, 64, 64, 64, 64, good, None, good, good, 0, None) == INV
     assert co(good, good, good, good, good, 64, 64, 64, 64, good, good, odd, good, 0, None) == MIS
     assert co(None, None, None, None, None, 0, 64, 64, 64, None, None, None, None, 2, None) == 0
+    # no output at all (no C and no cast) is refused; no C with a cast output is fine to validate
+    assert co(good, good, good, good, None, 64, 64, 64, 64, None, None, None, None, 0, None) == INV
+    assert co(good, good, good, good, None, 64, 64, 64, 0, good, good, odd, good, 0, None) == MIS
     st = ctypes.c_int(0)
     assert L.mxfp4_device_status(0, None) == INV
 

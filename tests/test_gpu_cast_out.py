@@ -97,6 +97,29 @@ def test_cast_out_degenerate_blocks(m):
     check_casts(c, qr, sr, qc, sc, False, True)
 
 
+@pytest.mark.parametrize("M,N,K", [(384, 288, 256), (8192, 4096, 1024)])
+def test_cast_out_without_c(m, M, N, K):
+    # the cast-only form (no bf16 C stored) writes the same casts as the full one
+    ca, sa, cb, sb = random_operands(M, N, K, seed=M + 2 * N + K)
+    full = run_cast_out(m, ca, sa, cb, sb, M, N, K, True, True, False, True)
+    args = [dev_u8(ca), dev_u8(oracle.sf_linear_to_tile(sa)), dev_u8(cb), dev_u8(oracle.sf_linear_to_tile(sb))]
+    c, qr, sr, qc, sc = m.gemm_fp4_cast_out(*args, M, N, K, hadamard_col=True, write_c=False)
+    torch.cuda.synchronize()
+    assert c is None
+    for got, want in zip((qr, sr, qc, sc), full[1:]):
+        assert torch.equal(got, want)
+    check_casts(full[0], qr, sr, qc, sc, False, True)
+
+
+def test_cast_out_k_zero_without_c(m):
+    e = torch.empty(0, dtype=torch.uint8, device="cuda")
+    c, qr, sr, qc, sc = m.gemm_fp4_cast_out(e, e, e, e, 96, 64, 0, hadamard_col=True, write_c=False)
+    torch.cuda.synchronize()
+    assert c is None
+    for t in (qr, sr, qc, sc):
+        assert torch.count_nonzero(t) == 0
+
+
 def test_cast_out_k_zero(m):
     M, N = 64, 96
     e = torch.empty(0, dtype=torch.uint8, device="cuda")

@@ -105,3 +105,48 @@ def test_quantizer_presets_match_the_dual_cast(L):
         assert np.array_equal(tq.sf_row.cpu().numpy(), oracle.sf_linear_to_tile(sr))
         assert np.array_equal(tq.q_col.cpu().numpy(), cc)
         assert np.array_equal(tq.sf_col.cpu().numpy(), oracle.sf_linear_to_tile(sc))
+
+
+def test_stack_matches_chain_of_layers(L):
+    # Layers back to back: the stack hands each GEMM its operand already cast
+    # (in the producing GEMM's epilogue), a chain of MXFP4Linear layers casts
+    # the bf16 tensors in between.  The fused casts equal the separate ones
+    # byte for byte, so output and every gradient must be identical.
+    dims = [128, 256, 96, 160]
+    M = 320
+    ws = [synth.normal_bf16((dims[i + 1], dims[i]), 0.05, seed=40 + i).cuda() for i in range(3)]
+    x = synth.normal_bf16((M, dims[0]), 1.0, seed=50).cuda()
+    dy = synth.normal_bf16((M, dims[-1]), 1e-2, seed=51).cuda()
+
+    stack = L.MXFP4LinearStack([w.clone() for w in ws])
+    xs = x.clone().requires_grad_(True)
+    ys = stack(xs)
+    ys.backward(dy)
+
+    layers = [L.MXFP4Linear(w.clone(), cache_name=f"l{i}") for i, w in enumerate(ws)]
+    xc = x.clone().requires_grad_(True)
+    h = xc
+    for layer in layers:
+        h = layer(h)
+    h.backward(dy)
+    torch.cuda.synchronize()
+
+    assert torch.equal(ys, h)
+    assert torch.equal(xs.grad, xc.grad)
+    for i, (p, layer) in enumerate(zip(stack.weights, layers)):
+        assert torch.equal(p.grad, layer.weight.grad), f"dW of layer {i}"
+
+
+def test_single_layer_stack_is_the_layer(L):
+    M, N, K = 256, 384, 512
+    w = synth.normal_bf16((N, K), 0.02, seed=60).cuda()
+    x = synth.normal_bf16((M, K), 1.0, seed=61).cuda()
+    dy = synth.normal_bf16((M, N), 1e-3, seed=62).cuda()
+    stack, layer = L.MXFP4LinearStack([w.clone()]), L.MXFP4Linear(w.clone())
+    xs, xl = x.clone().requires_grad_(True), x.clone().requires_grad_(True)
+    ys, yl = stack(xs), layer(xl)
+    ys.backward(dy)
+    yl.backward(dy)
+    torch.cuda.synchronize()
+    assert torch.equal(ys, yl) and torch.equal(xs.grad, xl.grad)
+    assert torch.equal(stack.weights[0].grad, layer.weight.grad)

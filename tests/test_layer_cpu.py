@@ -49,3 +49,17 @@ def test_presets():
     assert MXFP4Quantizer.for_grad().hadamard_col
     assert {MXFP4Quantizer.for_weight().role, MXFP4Quantizer.for_activation().role,
             MXFP4Quantizer.for_grad().role} == {"weight", "activation", "grad"}
+
+
+def test_stack_shape_validation():
+    import pytest
+    from quantization_mxfp4_cast_gb300.layer import MXFP4LinearStack
+    bf = lambda *s: torch.zeros(*s, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        MXFP4LinearStack([])
+    with pytest.raises(ValueError):
+        MXFP4LinearStack([bf(64, 32), bf(32, 96)])   # 96 inputs after 64 outputs
+    with pytest.raises(ValueError):
+        MXFP4LinearStack([bf(48, 32)])               # 48 is not a multiple of 32
+    s = MXFP4LinearStack([bf(64, 32), bf(96, 64)])
+    assert [tuple(p.shape) for p in s.weights] == [(64, 32), (96, 64)]
