@@ -99,6 +99,28 @@ def test_gemm_mxfp8_on_oracle_operands(m, M, N, K):
     assert m.device_status() == 0
 
 
+def test_gemm_mxfp8_partial_raster_group(m):
+    # The kernel walks the 256-row tiles in groups sized to K (8 row tiles for
+    # E4M3 at K = 8192): M = 2336 is 10 row tiles, ending in a group of 2,
+    # with a ragged last row and column tile.  Random E4M3 codes (the two NaN
+    # patterns replaced) and scales, against the oracle GEMM.
+    M, N, K = 2336, 264, 8192
+    rng = np.random.default_rng(2336)
+    ca = rng.integers(0, 256, size=(M, K), dtype=np.uint8)
+    cb = rng.integers(0, 256, size=(N, K), dtype=np.uint8)
+    ca[(ca & 0x7F) == 0x7F] = 0x3E
+    cb[(cb & 0x7F) == 0x7F] = 0xBE
+    sa = rng.integers(0x76, 0x7A, size=(M, K // 32), dtype=np.uint8)
+    sb = rng.integers(0x76, 0x7A, size=(N, K // 32), dtype=np.uint8)
+    c = m.gemm_mxfp8(to_dev(ca), to_dev(oracle.sf_linear_to_tile(sa)), to_dev(cb),
+                     to_dev(oracle.sf_linear_to_tile(sb)), M, N, K)
+    torch.cuda.synchronize()
+    ref = oracle.gemm_mxfp8(ca, sa, cb, sb, nthreads=8)
+    ok, excess = gemm_tolerance_ok(c.float().cpu().numpy(), ref)
+    assert ok, f"worst excess {excess:.3e}"
+    assert m.device_status() == 0
+
+
 @pytest.mark.parametrize("hadamard", [True, False])
 @pytest.mark.parametrize("M,N,K", [(256, 384, 320), (96, 64, 128), (320, 160, 224)])
 def test_fp8_wgrad(m, M, N, K, hadamard):
