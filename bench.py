@@ -71,10 +71,20 @@ def load_peaks():
                 "source": "fallback"}
 
 
+def strip_comments(src: str) -> str:
+    """C++ source without its comments and blank lines (the sources hold no
+    string literal with comment markers), so that a comment edit keeps the hash."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def gemm_source_hash():
+    """sha256[:16] of the GEMM's code (gemm.cu + ptx.cuh, comments stripped)."""
     h = hashlib.sha256()
     for f in ("gemm.cu", "ptx.cuh"):
-        h.update(open(os.path.join(ROOT, "quantization_mxfp4_cast_gb300", "csrc", f), "rb").read())
+        text = open(os.path.join(ROOT, "quantization_mxfp4_cast_gb300", "csrc", f)).read()
+        h.update(strip_comments(text).encode())
     return h.hexdigest()[:16]
 
 

@@ -20,7 +20,8 @@
 //     (a 256-element K slab is one 128-byte swizzle row) and the 512-byte
 //     scale tiles, which the cast already writes in the tensor-memory copy
 //     layout (B's two 128-row tiles in one 3-D box), into a 6-stage
-//     shared-memory ring (measured: 5 stages run as fast, 4 are 11% slower);
+//     shared-memory ring (measured: 4 stages are 11% slower; the 5-stage ring
+//     of the output-cast instance is 4-6% slower with no cast work);
 //   * warps 2-5, in each CTA: scale stagers -- each takes one 32-lane quarter
 //     of tensor memory and writes the stage's A and B scales there with
 //     tcgen05.st (the layout the block-scaled MMA reads: lane i of every
