@@ -208,7 +208,8 @@ class _MXFP4StackFn(torch.autograd.Function):
                 x_q = nxt
             else:
                 y = gemm_fp4(x_q.q_row, x_q.sf_row, w_q.q_row, w_q.sf_row, M, N, K, stream=stream)
-        ctx.acts, ctx.w_qs, ctx.shapes, ctx.M = acts, w_qs, [tuple(w.shape) for w in ws], M
+        if any(ctx.needs_input_grad):  # keep the quantized activations only for a backward
+            ctx.acts, ctx.w_qs, ctx.shapes, ctx.M = acts, w_qs, [tuple(w.shape) for w in ws], M
         return y
 
     @staticmethod
