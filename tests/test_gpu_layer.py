@@ -150,3 +150,15 @@ def test_single_layer_stack_is_the_layer(L):
     torch.cuda.synchronize()
     assert torch.equal(ys, yl) and torch.equal(xs.grad, xl.grad)
     assert torch.equal(stack.weights[0].grad, layer.weight.grad)
+
+
+def test_stack_inference_matches_training_forward(L):
+    dims = [64, 128, 96]
+    ws = [synth.normal_bf16((dims[i + 1], dims[i]), 0.05, seed=80 + i).cuda() for i in range(2)]
+    x = synth.normal_bf16((160, dims[0]), 1.0, seed=82).cuda()
+    stack = L.MXFP4LinearStack(ws)
+    y_train = stack(x.clone().requires_grad_(True))
+    with torch.no_grad():
+        y_infer = stack(x)
+    torch.cuda.synchronize()
+    assert torch.equal(y_train.detach(), y_infer)
