@@ -2,9 +2,13 @@
 
 Each .cu file compiles in parallel to an object, then one nvcc link step makes
 the shared library.  The result sits next to this file; nothing is installed.
+An object is rebuilt when its source or ANY header under csrc/ or include/ is
+newer than it (every translation unit may include every header, directly or
+not, so the headers are not tracked per file).
 """
 from __future__ import annotations
 
+import glob
 import os
 import shutil
 import subprocess
@@ -13,10 +17,10 @@ from concurrent.futures import ThreadPoolExecutor
 
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG_DIR, "csrc")
+INCLUDE = os.path.join(os.path.dirname(PKG_DIR), "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libmxfp4.so")
 SOURCES = ["cast.cu", "gemm.cu", "api.cu", "noalloc.cu"]
-HEADERS = ["ptx.cuh", "internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
@@ -30,6 +34,15 @@ def nvcc() -> str:
     return cand
 
 
+def headers(csrc: str = CSRC, include: str = INCLUDE) -> list:
+    """Every header a translation unit may include."""
+    found = []
+    for d in (csrc, include):
+        for pat in ("*.h", "*.cuh", "*.hpp"):
+            found += glob.glob(os.path.join(d, pat))
+    return sorted(found)
+
+
 def _stale(target: str, deps) -> bool:
     if not os.path.exists(target):
         return True
@@ -37,18 +50,25 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def stale_sources(csrc: str = CSRC, include: str = INCLUDE, build_dir: str = BUILD_DIR,
+                  sources=SOURCES, force: bool = False) -> list:
+    """The sources whose object must be recompiled."""
+    hdrs = headers(csrc, include)
+    out = []
+    for src in sources:
+        s = os.path.join(csrc, src)
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
+        if force or _stale(o, [s] + hdrs):
+            out.append(src)
+    return out
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
-    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [
-        os.path.join(os.path.dirname(PKG_DIR), "include", "mxfp4.h")]
-    objs = []
-    jobs = []
-    for src in SOURCES:
-        s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        objs.append(o)
-        if force or _stale(o, [s] + hdrs):
-            jobs.append([nvcc(), *ARCH, *NVCC_FLAGS, "-c", s, "-o", o])
+    objs = [os.path.join(BUILD_DIR, src.replace(".cu", ".o")) for src in SOURCES]
+    jobs = [[nvcc(), *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o",
+             os.path.join(BUILD_DIR, src.replace(".cu", ".o"))]
+            for src in stale_sources(force=force)]
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)

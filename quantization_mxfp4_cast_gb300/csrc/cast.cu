@@ -11,28 +11,43 @@
 //
 // Design (HBM-bound: 2 bytes read, ~0.53 bytes written per element per
 // direction; the arithmetic is kept to a few instructions per element so the
-// ALU pipes stay below the memory rate):
-//   * persistent CTAs (as many as fit on the GPU), 256 threads each, walking
-//     128 x 128 tiles of x; each tile arrives in shared memory by two TMA
-//     loads (64-column halves, 128-byte swizzle, zero fill past the edges)
-//     into a double buffer, so the next tile's load overlaps this tile's
-//     arithmetic and stores;
-//   * row pass: from the shared-memory tile, one lane per 32-element block
-//     (four 16-byte reads, conflict-free because of the swizzle); block amax
-//     as a tree of packed, NaN-propagating bf16 magnitude maxima; the
-//     power-of-two scaling as an exact bf16x2 multiply; packing by
-//     cvt.rn.satfinite.e2m1x2.f32 (which keeps the sign of values that round
-//     to zero); the row-wise Hadamard in registers;
-//   * column pass: from the same shared-memory tile (untransformed); each
-//     thread takes a column pair x 32 rows (conflict-free 4-byte reads) and
-//     treats the two columns as the two halves of packed words -- one packed
-//     max per row gives both amaxes, one bf16x2 multiply scales both, and the column
-//     Hadamard runs both columns through one f32x2 butterfly network; 16
-//     bytes of codes are stored per column;
-//   * a 128 x 128 tile owns exactly one 512-byte scale tile of each output
-//     (128 rows x 4 blocks), assembled in shared memory (double-buffered, so
-//     one barrier per tile suffices) and written with one coalesced store,
-//     padding included.
+// issue slots stay below the memory rate):
+//   * the work unit is a slab of 32 rows x 128 columns (8 KB of bf16) that ONE
+//     warp quantizes completely -- its 128 row blocks and its 128 column
+//     blocks -- so no warp waits for another one to finish a tile;
+//   * one persistent CTA per SM owns the 128 x 128 tiles blockIdx.x + k *
+//     gridDim.x.  A producer thread streams their slabs with TMA (two 32 x 64
+//     boxes, 128-byte swizzle, zero fill past the edges) into a ring of 24
+//     slots; 15 consumer warps take the slabs in order from a shared counter
+//     as they become free, so the four slabs of a tile are quantized side by
+//     side (balanced to within one slab per SM, with loads in flight beyond the
+//     slabs being quantized).  A slot's sequence word tells a consumer when
+//     the producer has claimed the slot for its slab (and publishes the
+//     slab's coordinates), so no consumer waits on a barrier phase that
+//     belongs to an earlier use of the slot;
+//   * the four 16-byte column-code pieces of a tile's column are written by
+//     those four warps at nearly the same time (measured: when the pieces of
+//     a 64-byte run came from different SMs at different times, the stores
+//     took ~2.5x as long), and a tile's two 512-byte scale tiles are
+//     assembled in shared memory and written whole by the warp that finishes
+//     the tile's last slab;
+//   * row blocks: lane l takes row 8i + l % 8 (i = 0..3), block l / 8, read as
+//     four 16-byte chunks (conflict-free under the swizzle); a store
+//     instruction writes 8 rows x 64 contiguous bytes;
+//   * column blocks: each lane takes two column pairs x 32 rows as the halves
+//     of packed 4-byte words (conflict-free reads), so one packed max gives
+//     both amaxes and one f32x2 butterfly network transforms both columns;
+//   * block amax as a tree of packed, NaN-propagating bf16 magnitude maxima;
+//     scaling by the exact power of two with the mixed-precision fma (or the
+//     fused 1/sqrt(32) * 2^-e multiply after the transform, where that is
+//     exact); packing by cvt.rn.satfinite.e2m1x2.f32, which keeps the sign of
+//     values that round to zero;
+//   * row blocks are padded to whole 128-row tiles (slabs past the last row
+//     are zero fill), so every byte of every scale tile, padding included, is
+//     written (0x00 for padding);
+//   * launched with programmatic stream serialization: the barrier set-up
+//     overlaps the end of the previous kernel in the stream, and every read of
+//     x and write of an output waits for that kernel to complete.
 #include <algorithm>
 #include <atomic>
 
@@ -43,8 +58,19 @@
 namespace mxfp4 {
 namespace {
 
-constexpr int kTile = 128;
-constexpr int kThreads = 256;
+constexpr int kSlabRows = 32;
+constexpr int kSlabCols = 128;
+constexpr int kHalfBytes = kSlabRows * 128;  // one 64-column half: 32 rows x 128 bytes
+constexpr int kSlabBytes = 2 * kHalfBytes;   // 8 KB
+constexpr int kStages = 24;                  // ring slots
+constexpr int kConsumerWarps = 15;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + the producer warp
+constexpr int kSfBufs = 12;                  // scale-tile staging buffers (tiles in progress)
+constexpr int kSfStageBytes = 2 * 512;       // one tile's row and column scale tiles
+constexpr int kBarrierBytes = 2 * kStages * 8 + 3 * kStages * 4 + 2 * kSfBufs * 4 + 16;
+constexpr int kCastSmemBytes = kStages * kSlabBytes + kSfBufs * kSfStageBytes + kBarrierBytes + 1024;
+static_assert(kStages % 4 == 0, "a tile's four slabs take four consecutive ring slots");
+constexpr uint32_t kNoSlab = 0xFFFFFFFFu;
 
 // E4M3 codes of 4 values, element 0 in the low byte.  The conversion rounds
 // to nearest even and saturates at +-448 (cvt puts its first source in the
@@ -75,315 +101,372 @@ __device__ __forceinline__ void block_codes(V v, uint32_t* out) {
   }
 }
 
-__device__ __forceinline__ int sf_in_tile(int r, int b) { return (r & 31) * 16 + (r >> 5) * 4 + b; }
+// Byte of (row r, block b) inside a 512-byte scale tile of 128 rows x 4 blocks.
+__device__ __forceinline__ int sf_in_tile(int r, int b) { return (r & 31) * 16 + ((r >> 5) & 3) * 4 + b; }
 
-// A 128 x 128 bf16 tile in shared memory is two 128-row halves of 64 columns
-// (128 bytes per row), each written by one TMA load with the 128-byte
-// swizzle: the 16-byte chunk k of row r sits at chunk position k ^ (r % 8).
-// Both passes below read it without bank conflicts: eight lanes reading the
-// same chunk of eight consecutive rows, or 32 lanes reading 4-byte words of
-// one row, always land on distinct banks.
-constexpr int kHalfBytes = kTile * 128;
-constexpr int kTileBytes = 2 * kHalfBytes;
-constexpr int kSfTileBytes = 512;
-constexpr int kCastSmemBytes = 2 * kTileBytes + 4 * kSfTileBytes + 64 + 1024;
-
-template <bool kRow, bool kCol, bool kFp8>
-__global__ void __launch_bounds__(kThreads, 3)
-    cast_kernel(const __grid_constant__ CUtensorMap tmX, const CastArgs args, int col_tiles,
-                int num_tiles, int* status) {
-  extern __shared__ uint8_t smem_raw[];
-  // 1024-byte alignment: the swizzle pattern follows address bits 7..9.
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* bufs = smem;                               // two tiles
-  uint8_t* sf_row_tiles = smem + 2 * kTileBytes;      // two 512-byte scale tiles (row output)
-  uint8_t* sf_col_tiles = sf_row_tiles + 2 * kSfTileBytes;  // two (column output)
-  uint64_t* full = reinterpret_cast<uint64_t*>(sf_col_tiles + 2 * kSfTileBytes);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
-
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-  const int64_t rows = args.rows, cols = args.cols;
-  const bool linear = (args.flags & kFlagScaleLinear) != 0;
-
-  if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  __syncthreads();
-  // Tile t covers rows 128 * (t / col_tiles), columns 128 * (t % col_tiles).
-  // The TMA zero-fills whatever lies past the tensor's edge (including a
-  // half that starts beyond the last column).
-  auto issue = [&](int t, int b) {
-    const int x = (t % col_tiles) * kTile, y = (t / col_tiles) * kTile;
-    uint8_t* dst = bufs + b * kTileBytes;
-    mbar_arrive_expect_tx(&full[b], kTileBytes);
-    tma_load_2d(dst, &tmX, &full[b], x, y);
-    tma_load_2d(dst + kHalfBytes, &tmX, &full[b], x + kTile / 2, y);
-  };
-  if (tid == 0) {
-    tma_prefetch_desc(&tmX);
-    for (int b = 0; b < 2; ++b) {
-      const int t = static_cast<int>(blockIdx.x) + b * static_cast<int>(gridDim.x);
-      if (t < num_tiles) issue(t, b);
-    }
-  }
-
-  // Tile coordinates advance by the grid size each step.
-  int tile_x = static_cast<int>(blockIdx.x) % col_tiles;
-  int tile_y = static_cast<int>(blockIdx.x) / col_tiles;
-  const int step_x = static_cast<int>(gridDim.x) % col_tiles;
-  const int step_y = static_cast<int>(gridDim.x) / col_tiles;
-
-  int it = 0;
-  for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
-  const int b = it & 1;
-  if (!mbar_wait(&full[b], (it >> 1) & 1, abort_flag, status)) break;
-  const uint8_t* tile = bufs + b * kTileBytes;
-  const int64_t c0 = static_cast<int64_t>(tile_x) * kTile;
-  const int64_t r0 = static_cast<int64_t>(tile_y) * kTile;
-  uint8_t* sf_row_tile = sf_row_tiles + b * kSfTileBytes;
-  uint8_t* sf_col_tile = sf_col_tiles + b * kSfTileBytes;
-
-  static_assert(!(kFp8 && kRow), "MXFP8 is produced column-wise only");
-  // ---------------------------------------------------------------- row pass
-  // One lane per 32-element block: warp w, lane l take tile row
-  // 8 w + (l % 8) (+ 64 in the second iteration), block l / 8 of that row.
-  if constexpr (kRow) {
-    const bool had = (args.flags & kFlagHadamardRow) != 0;
-    const int kb = lane >> 3;
-    const int xk = ((kb & 1) * 4) ^ (lane & 7);  // chunk 4 (kb % 2) + j sits at xk ^ j
-    const bool col_ok = c0 + kb * 32 < cols;      // cols is a multiple of 32
-#pragma unroll
-    for (int ri = 0; ri < 2; ++ri) {
-      const int row = warp * 8 + (lane & 7) + ri * 64;
-      const uint8_t* rowp = tile + (kb >> 1) * kHalfBytes + row * 128;
-      uint32_t v[16];  // elements 2i (low half), 2i + 1 of the block
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 q = *reinterpret_cast<const uint4*>(rowp + ((xk ^ j) << 4));
-        v[4 * j] = q.x;
-        v[4 * j + 1] = q.y;
-        v[4 * j + 2] = q.z;
-        v[4 * j + 3] = q.w;
-      }
-      uint4 codes;
-      BlockScale s;
-      if (!had) {
-        uint32_t m = tree_absmax_bf16x2<16>(v);
-        m = absmax_bf16x2(m, __byte_perm(m, 0, 0x1032));  // both halves hold the block max
-        s = block_scale((m & 0x7FFFu) << 16);
-        const uint16_t mb = static_cast<uint16_t>(s.mult_bf16);
-        codes.x = quantize8_bf16(v[0], v[1], v[2], v[3], mb);
-        codes.y = quantize8_bf16(v[4], v[5], v[6], v[7], mb);
-        codes.z = quantize8_bf16(v[8], v[9], v[10], v[11], mb);
-        codes.w = quantize8_bf16(v[12], v[13], v[14], v[15], mb);
-        if (s.nonfinite) codes = make_uint4(0u, 0u, 0u, 0u);
-      } else {
-        float y[32];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          y[2 * i] = bf16_times<false>(v[i], kBf16One);
-          y[2 * i + 1] = bf16_times<true>(v[i], kBf16One);
-        }
-#pragma unroll
-        for (int h = 1; h < 32; h <<= 1) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (j & h) continue;
-            const float a = y[j], c = y[j + h];
-            y[j] = __fadd_rn(a, c);
-            y[j + h] = __fsub_rn(a, c);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) y[j] = __fmul_rn(y[j], kInvSqrt32);
-        s = block_scale(__float_as_uint(amax32([&](int i) { return y[i]; })));
-        codes.x = quantize8(y, s);
-        codes.y = quantize8(y + 8, s);
-        codes.z = quantize8(y + 16, s);
-        codes.w = quantize8(y + 24, s);
-      }
-      const int64_t grow = r0 + row;
-      if (col_ok && grow < rows)
-        *reinterpret_cast<uint4*>(args.q_row + grow * (cols / 2) + (c0 + kb * 32) / 2) = codes;
-      if (linear) {
-        if (col_ok && grow < rows) args.sf_row[grow * (cols / 32) + (c0 / 32) + kb] = (uint8_t)s.byte;
-      } else {
-        sf_row_tile[sf_in_tile(row, kb)] = (uint8_t)s.byte;
+// Bounded wait until a shared word holds `want` (acquire).  The polls back
+// off with a short sleep, so that waiting warps leave the issue slots to the
+// producer and to the warps that have data.
+__device__ __forceinline__ bool wait_word(const uint32_t* p, uint32_t want, volatile int* abort_flag,
+                                          int* status_word) {
+  if (ld_acquire_shared(p) == want) return true;
+  const unsigned long long t0 = global_timer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    __nanosleep(64);
+    if (ld_acquire_shared(p) == want) return true;
+    if ((++spins & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicExch(status_word, 6 /* MXFP4_ERR_TIMEOUT */);
+        return false;
       }
     }
-  }
-
-  // ---------------------------------------------------------------- column pass
-  if constexpr (kCol) {
-    const bool had = (args.flags & kFlagHadamardCol) != 0;
-    const int p = tid & 63;   // column pair: tile columns 2p (low halves), 2p+1 (high halves)
-    const int rb = tid >> 6;  // 32-row block of the tile
-    const uint8_t* colp = tile + (p >> 5) * kHalfBytes + rb * 32 * 128 + (p & 3) * 4;
-    const int ch = (p & 31) >> 2;  // 16-byte chunk of the pair within its row half
-    uint32_t w[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      w[i] = *reinterpret_cast<const uint32_t*>(colp + i * 128 + ((ch ^ (i & 7)) << 4));
-    const bool rows_ok = r0 + rb * 32 < rows;  // rows is a multiple of 32
-    // MXFP4: 16 code bytes per column block; MXFP8 (E4M3, column output only): 32
-    constexpr int kWords = kFp8 ? 8 : 4;
-    constexpr int kEmax = kFp8 ? 8 : 2;
-    BlockScale sa, sb;
-    uint32_t ca[kWords], cb[kWords];  // codes of column 2p and 2p+1
-    if (!had) {
-      const uint32_t m = tree_absmax_bf16x2<32>(w) & 0x7FFF7FFFu;
-      sa = block_scale<kEmax>(m << 16);
-      sb = block_scale<kEmax>(m & 0xFFFF0000u);
-      const uint16_t ma = static_cast<uint16_t>(sa.mult_bf16), mb = static_cast<uint16_t>(sb.mult_bf16);
-      block_codes<kFp8>([&](int i) { return bf16_times<false>(w[i], ma); }, ca);
-      block_codes<kFp8>([&](int i) { return bf16_times<true>(w[i], mb); }, cb);
-    } else {
-      // both columns through one 32-point butterfly network on fp32 pairs
-      uint64_t y[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) y[i] = pk2(bf16_times<false>(w[i], kBf16One), bf16_times<true>(w[i], kBf16One));
-#pragma unroll
-      for (int h = 1; h < 32; h <<= 1) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (j & h) continue;
-          const uint64_t a = y[j], c = y[j + h];
-          y[j] = add2(a, c);
-          y[j + h] = sub2(a, c);
-        }
-      }
-      // amax of the transformed block: rounding is monotonic, so the largest
-      // |RN(h * c)| is RN(max |h| * c); the NaN-propagating max keeps NaN/Inf.
-      const float ha = amax32([&](int i) { return lo2(y[i]); });
-      const float hb = amax32([&](int i) { return hi2(y[i]); });
-      sa = block_scale<kEmax>(__float_as_uint(__fmul_rn(ha, kInvSqrt32)));
-      sb = block_scale<kEmax>(__float_as_uint(__fmul_rn(hb, kInvSqrt32)));
-      // v = RN(h * c) * 2^-e.  RN(h * (c * 2^-e)) is the same number when
-      // c * 2^-e stays normal (scale byte <= 250) and every transformed value
-      // RN(h * c) that is subnormal in fp32 (< 2^-126, so |v| < 2^(1 - byte))
-      // lands below the format's zero threshold either way: byte >= 3 for
-      // E2M1 (|v| < 1/4), byte >= 11 for E4M3 (|v| <= 2^-10).  Outside that
-      // range the two roundings are kept apart.
-      constexpr uint32_t kFusedMin = kFp8 ? 11u : 3u;
-      if ((sa.byte - kFusedMin) <= 250u - kFusedMin && (sb.byte - kFusedMin) <= 250u - kFusedMin) {
-        const uint64_t m2 = pk2(__fmul_rn(kInvSqrt32, sa.mult), __fmul_rn(kInvSqrt32, sb.mult));
-#pragma unroll
-        for (int i = 0; i < 32; ++i) y[i] = mul2(y[i], m2);
-      } else {
-        const uint64_t c2 = pk2(kInvSqrt32, kInvSqrt32);
-        const uint64_t m2 = pk2(sa.mult, sb.mult);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) y[i] = mul2(mul2(y[i], c2), m2);
-      }
-      block_codes<kFp8>([&](int i) { return lo2(y[i]); }, ca);
-      block_codes<kFp8>([&](int i) { return hi2(y[i]); }, cb);
-    }
-    if (sa.nonfinite) {
-#pragma unroll
-      for (int g = 0; g < kWords; ++g) ca[g] = 0u;
-    }
-    if (sb.nonfinite) {
-#pragma unroll
-      for (int g = 0; g < kWords; ++g) cb[g] = 0u;
-    }
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int c = 2 * p + half;
-      const BlockScale& s = half ? sb : sa;
-      const uint32_t* cw = half ? cb : ca;
-      const int64_t gcol = c0 + c;
-      if (gcol < cols && rows_ok) {
-        // codes of T^T: [cols, rows] bytes (MXFP8) or [cols, rows / 2] (MXFP4)
-        uint4* dst = reinterpret_cast<uint4*>(args.q_col + (gcol * rows + r0 + rb * 32) / (kFp8 ? 1 : 2));
-        dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        if constexpr (kFp8) dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-      }
-      if (linear) {
-        if (gcol < cols && rows_ok) args.sf_col[gcol * (rows / 32) + (r0 / 32) + rb] = (uint8_t)s.byte;
-      } else {
-        sf_col_tile[sf_in_tile(c, rb)] = (uint8_t)s.byte;
-      }
-    }
-  }
-
-  // ---------------------------------------------------------------- scale tiles
-  // One barrier per tile: the tile buffer is consumed and both scale tiles
-  // are complete.  The scale tiles are double-buffered, so the next tile's
-  // passes write the other pair while warps 0 and 1 copy these out; the
-  // pair is reused only after the next tile's barrier, which those warps
-  // reach after their copies.
-  __syncthreads();
-  if (tid == 0) {
-    const int tn = t + 2 * static_cast<int>(gridDim.x);
-    if (tn < num_tiles) {
-      fence_proxy_async_shared();  // order this tile's generic reads before the async refill
-      issue(tn, b);
-    }
-  }
-  if (!linear) {
-    if constexpr (kRow) {
-      if (warp == 0) {
-        const int64_t ktiles = (cols + kTile - 1) / kTile;
-        const int64_t tile_idx = static_cast<int64_t>(tile_y) * ktiles + tile_x;
-        reinterpret_cast<uint4*>(args.sf_row + tile_idx * 512)[lane] =
-            reinterpret_cast<const uint4*>(sf_row_tile)[lane];
-      }
-    }
-    if constexpr (kCol) {
-      if (warp == 1) {
-        const int64_t ktiles = (rows + kTile - 1) / kTile;
-        const int64_t tile_idx = static_cast<int64_t>(tile_x) * ktiles + tile_y;
-        reinterpret_cast<uint4*>(args.sf_col + tile_idx * 512)[lane] =
-            reinterpret_cast<const uint4*>(sf_col_tile)[lane];
-      }
-    }
-  }
-  tile_x += step_x;
-  tile_y += step_y;
-  if (tile_x >= col_tiles) {
-    tile_x -= col_tiles;
-    ++tile_y;
-  }
   }
 }
 
-}  // namespace
+// The CTA takes the 128 x 128 tiles t = blockIdx.x + k * gridDim.x (k = 0,
+// 1, ...) of x; tile t covers rows 128 * (t / col_tiles) and columns
+// 128 * (t % col_tiles).  Its local slab i = 4k + j is the tile's 32-row block
+// j, so the four slabs of a tile are handed out one after the other and
+// quantized side by side by four warps: the column codes of a tile's column
+// (four 16-byte pieces) are written together, and its two 512-byte scale
+// tiles are assembled in shared memory and written whole by the warp that
+// finishes the tile's last slab.
+template <bool kRow, bool kCol, bool kFp8, bool kHadRow, bool kHadCol>
+__global__ void __launch_bounds__(kThreads, 1)
+    cast_kernel(const __grid_constant__ CUtensorMap tmX, const CastArgs args, int col_tiles,
+                int row_tiles128, int num_tiles, int* status) {
+  static_assert(!(kFp8 && kRow), "MXFP8 is produced column-wise only");
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment: the swizzle pattern follows address bits 7..9.
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* ring = smem;
+  uint8_t* sf_stage = smem + kStages * kSlabBytes;  // [kSfBufs][row tile, column tile]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sf_stage + kSfBufs * kSfStageBytes);
+  uint64_t* empty = full + kStages;
+  uint32_t* seq = reinterpret_cast<uint32_t*>(empty + kStages);  // local slab that owns each slot
+  uint32_t* slot_rb = seq + kStages;                                // its 32-row block
+  uint32_t* slot_ct = slot_rb + kStages;                            // its 128-column tile
+  uint32_t* sf_free = slot_ct + kStages;   // staging buffer b is free for local tile sf_free[b]
+  int* tile_done = reinterpret_cast<int*>(sf_free + kSfBufs);      // slabs of the tile in b finished
+  int* counter = tile_done + kSfBufs;                                // next local slab to hand out
+  volatile int* abort_flag = counter + 1;
 
-namespace {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = args.rows, cols = args.cols;
+  const bool linear = (args.flags & kFlagScaleLinear) != 0;
+  // local slabs of this CTA: four per tile
+  const int n_local =
+      4 * static_cast<int>((static_cast<int64_t>(num_tiles) - blockIdx.x + gridDim.x - 1) / gridDim.x);
 
-template <bool kRow, bool kCol, bool kFp8 = false>
-cudaError_t launch_cast_t(const CUtensorMap& tm, const CastArgs& args, int col_tiles, int num_tiles,
-                          int dev, cudaStream_t stream) {
-  static std::atomic<int> ctas_per_sm[64];
-  int per_sm = (dev >= 0 && dev < 64) ? ctas_per_sm[dev].load(std::memory_order_relaxed) : 0;
-  if (per_sm == 0) {
-    cudaError_t e = cudaFuncSetAttribute(cast_kernel<kRow, kCol, kFp8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kCastSmemBytes);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      seq[s] = kNoSlab;
+    }
+    for (int b = 0; b < kSfBufs; ++b) {
+      sf_free[b] = static_cast<uint32_t>(b);
+      tile_done[b] = 0;
+    }
+    *counter = 0;
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 32 * kConsumerWarps) tma_prefetch_desc(&tmX);
+  __syncthreads();
+  // x may be the output of the previous kernel in the stream, and the outputs
+  // may still be read by it: nothing below touches global memory before it ends.
+  grid_dependency_wait();
+  grid_launch_dependents();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      // tile coordinates advance by the grid size each step (no divisions in the loop)
+      int tx = static_cast<int>(blockIdx.x) % col_tiles, ty = static_cast<int>(blockIdx.x) / col_tiles;
+      const int step_x = static_cast<int>(gridDim.x) % col_tiles, step_y = static_cast<int>(gridDim.x) / col_tiles;
+      int slot = 0;
+      uint32_t empty_parity = 1;  // from the second pass on: parity of the slot's previous release
+      bool ok = true;
+      for (int i = 0; ok && i < n_local; i += 4) {
+        for (int j = 0; j < 4; ++j) {
+          // the slot's previous slab (i + j - kStages) has been quantized
+          if (i + j >= kStages && !mbar_wait(&empty[slot], empty_parity, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          const int rb = 4 * ty + j;
+          slot_rb[slot] = static_cast<uint32_t>(rb);
+          slot_ct[slot] = static_cast<uint32_t>(tx);
+          st_release_shared(&seq[slot], static_cast<uint32_t>(i + j));  // publishes the coordinates too
+          uint8_t* dst = ring + slot * kSlabBytes;
+          mbar_arrive_expect_tx(&full[slot], kSlabBytes);
+          tma_load_2d(dst, &tmX, &full[slot], tx * kSlabCols, rb * kSlabRows);
+          tma_load_2d(dst + kHalfBytes, &tmX, &full[slot], tx * kSlabCols + kSlabCols / 2, rb * kSlabRows);
+          issued = i + j + 1;
+          if (++slot == kStages) {
+            slot = 0;
+            empty_parity ^= 1u;
+          }
+        }
+        tx += step_x;
+        ty += step_y;
+        if (tx >= col_tiles) {
+          tx -= col_tiles;
+          ++ty;
+        }
+      }
+      // Every load issued has landed before the CTA may end (a consumer that
+      // gave up may have left one unconsumed).  The last load into a slot
+      // completes the phase its slab index gives; nothing follows it.
+      volatile int keep_waiting = 0;  // not the CTA's abort flag: this wait must run its course
+      for (int sl = 0; sl < kStages && sl < issued; ++sl) {
+        const int last = sl + ((issued - 1 - sl) / kStages) * kStages;
+        mbar_wait(&full[sl], (last / kStages) & 1, &keep_waiting, status);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  for (;;) {
+    int i = 0;
+    if (lane == 0) i = atomicAdd(counter, 1);
+    i = __shfl_sync(0xFFFFFFFFu, i, 0);
+    if (i >= n_local) break;
+    const int slot = i % kStages;
+    if (!wait_word(&seq[slot], static_cast<uint32_t>(i), abort_flag, status)) break;
+    const int rb = static_cast<int>(slot_rb[slot]);  // 32-row block (published with seq)
+    const int ct = static_cast<int>(slot_ct[slot]);
+    const int sfb = (i >> 2) % kSfBufs;                // this tile's scale staging buffer
+    uint8_t* sf_row_stage = sf_stage + sfb * kSfStageBytes;
+    uint8_t* sf_col_stage = sf_row_stage + 512;
+    if (!linear && !wait_word(&sf_free[sfb], static_cast<uint32_t>(i >> 2), abort_flag, status)) break;
+    if (!mbar_wait(&full[slot], (i / kStages) & 1, abort_flag, status)) break;
+    const uint8_t* tile = ring + slot * kSlabBytes;
+    const int64_t c0 = static_cast<int64_t>(ct) * kSlabCols;
+    const int64_t r0 = static_cast<int64_t>(rb) * kSlabRows;
+
+    // ---------------------------------------------------------- row blocks
+    if constexpr (kRow) {
+      const int kb = lane >> 3;
+      const int xk = ((kb & 1) * 4) ^ (lane & 7);  // chunk 4 (kb % 2) + j sits at xk ^ j
+      const bool col_ok = c0 + kb * 32 < cols;      // cols is a multiple of 32
+      const uint8_t* half = tile + (kb >> 1) * kHalfBytes;
+#pragma unroll 1
+      for (int it = 0; it < 4; ++it) {
+        const int row = it * 8 + (lane & 7);
+        const uint8_t* rowp = half + row * 128;
+        uint32_t v[16];  // elements 2i (low half), 2i + 1 of the block
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 q = *reinterpret_cast<const uint4*>(rowp + ((xk ^ j) << 4));
+          v[4 * j] = q.x;
+          v[4 * j + 1] = q.y;
+          v[4 * j + 2] = q.z;
+          v[4 * j + 3] = q.w;
+        }
+        uint32_t c[4];
+        BlockScale sc;
+        if constexpr (!kHadRow) {
+          sc = quantize_bf16_block(v, c);
+        } else {
+          float y[32];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            y[2 * k] = __uint_as_float(v[k] << 16);
+            y[2 * k + 1] = __uint_as_float(v[k] & 0xFFFF0000u);
+          }
+          sc = quantize_hadamard_block(y, c);
+        }
+        const int64_t grow = r0 + row;
+        if (col_ok && grow < rows)
+          *reinterpret_cast<uint4*>(args.q_row + grow * (cols / 2) + (c0 + kb * 32) / 2) =
+              make_uint4(c[0], c[1], c[2], c[3]);
+        if (linear) {
+          if (col_ok && grow < rows) args.sf_row[grow * (cols / 32) + (c0 / 32) + kb] = (uint8_t)sc.byte;
+        } else {
+          sf_row_stage[sf_in_tile(rb * 32 + row, kb)] = (uint8_t)sc.byte;
+        }
+      }
+    }
+
+    // ---------------------------------------------------------- column blocks
+    if constexpr (kCol) {
+      const bool rows_ok = r0 < rows;  // rows is a multiple of 32
+      const int ch = lane >> 2;        // 16-byte chunk of the pair within its row half
+      // MXFP4: 16 code bytes per column block; MXFP8 (E4M3, column output only): 32
+      constexpr int kWords = kFp8 ? 8 : 4;
+      constexpr int kEmax = kFp8 ? 8 : 2;
+#pragma unroll 1
+      for (int hp = 0; hp < 2; ++hp) {
+        const uint8_t* colp = tile + hp * kHalfBytes + (lane & 3) * 4;
+        uint32_t w[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          w[k] = *reinterpret_cast<const uint32_t*>(colp + k * 128 + ((ch ^ (k & 7)) << 4));
+        BlockScale sa, sb;
+        uint32_t ca[kWords], cb[kWords];  // codes of columns 2p and 2p + 1
+        if constexpr (!kHadCol) {
+          const uint32_t m = tree_absmax_bf16x2<32>(w) & 0x7FFF7FFFu;
+          sa = block_scale<kEmax>(m << 16);
+          sb = block_scale<kEmax>(m & 0xFFFF0000u);
+          const uint16_t ma = static_cast<uint16_t>(sa.mult_bf16), mb = static_cast<uint16_t>(sb.mult_bf16);
+          block_codes<kFp8>([&](int k) { return bf16_times<false>(w[k], ma); }, ca);
+          block_codes<kFp8>([&](int k) { return bf16_times<true>(w[k], mb); }, cb);
+        } else {
+          // both columns through one 32-point butterfly network on fp32 pairs
+          uint64_t y[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) y[k] = pk2(bf16_times<false>(w[k], kBf16One), bf16_times<true>(w[k], kBf16One));
+#pragma unroll
+          for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (j & h) continue;
+              const uint64_t a = y[j], c = y[j + h];
+              y[j] = add2(a, c);
+              y[j + h] = sub2(a, c);
+            }
+          }
+          // amax of the transformed block: rounding is monotonic, so the largest
+          // |RN(h * c)| is RN(max |h| * c); the NaN-propagating max keeps NaN/Inf.
+          const float ha = amax32([&](int k) { return lo2(y[k]); });
+          const float hb = amax32([&](int k) { return hi2(y[k]); });
+          sa = block_scale<kEmax>(__float_as_uint(__fmul_rn(ha, kInvSqrt32)));
+          sb = block_scale<kEmax>(__float_as_uint(__fmul_rn(hb, kInvSqrt32)));
+          // v = RN(h * c) * 2^-e.  RN(h * (c * 2^-e)) is the same number when
+          // c * 2^-e stays normal (scale byte <= 250) and every transformed value
+          // RN(h * c) that is subnormal in fp32 (< 2^-126, so |v| < 2^(1 - byte))
+          // lands below the format's zero threshold either way: byte >= 3 for
+          // E2M1 (|v| < 1/4), byte >= 11 for E4M3 (|v| <= 2^-10).  Outside that
+          // range the two roundings are kept apart.
+          constexpr uint32_t kFusedMin = kFp8 ? 11u : 3u;
+          if ((sa.byte - kFusedMin) <= 250u - kFusedMin && (sb.byte - kFusedMin) <= 250u - kFusedMin) {
+            const uint64_t m2 = pk2(__fmul_rn(kInvSqrt32, sa.mult), __fmul_rn(kInvSqrt32, sb.mult));
+#pragma unroll
+            for (int k = 0; k < 32; ++k) y[k] = mul2(y[k], m2);
+          } else {
+            const uint64_t c2 = pk2(kInvSqrt32, kInvSqrt32);
+            const uint64_t m2 = pk2(sa.mult, sb.mult);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) y[k] = mul2(mul2(y[k], c2), m2);
+          }
+          block_codes<kFp8>([&](int k) { return lo2(y[k]); }, ca);
+          block_codes<kFp8>([&](int k) { return hi2(y[k]); }, cb);
+        }
+        if (sa.nonfinite) {
+#pragma unroll
+          for (int g = 0; g < kWords; ++g) ca[g] = 0u;
+        }
+        if (sb.nonfinite) {
+#pragma unroll
+          for (int g = 0; g < kWords; ++g) cb[g] = 0u;
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int c = 64 * hp + 2 * lane + half;  // column within the slab
+          const BlockScale& sc = half ? sb : sa;
+          const uint32_t* cw = half ? cb : ca;
+          const int64_t gcol = c0 + c;
+          if (gcol < cols && rows_ok) {
+            // codes of T^T: [cols, rows] bytes (MXFP8) or [cols, rows / 2] (MXFP4)
+            uint4* dst = reinterpret_cast<uint4*>(args.q_col + (gcol * rows + r0) / (kFp8 ? 1 : 2));
+            dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+            if constexpr (kFp8) dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+          }
+          if (linear) {
+            if (gcol < cols && rows_ok) args.sf_col[gcol * (rows / 32) + rb] = (uint8_t)sc.byte;
+          } else {
+            sf_col_stage[sf_in_tile(c, rb & 3)] = (uint8_t)sc.byte;
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);  // the slot may be refilled
+    if (!linear) {
+      // the warp that finishes the tile's last slab writes its scale tiles
+      int done = 0;
+      if (lane == 0) {
+        __threadfence_block();  // this warp's staging bytes before the count
+        done = atomicAdd(&tile_done[sfb], 1);
+      }
+      if (__shfl_sync(0xFFFFFFFFu, done, 0) == 3) {
+        __threadfence_block();  // the other three warps' staging bytes
+        const size_t tile_y = static_cast<size_t>(rb >> 2), tile_x = static_cast<size_t>(ct);
+        if constexpr (kRow)
+          reinterpret_cast<uint4*>(args.sf_row + (tile_y * col_tiles + tile_x) * 512)[lane] =
+              reinterpret_cast<const uint4*>(sf_row_stage)[lane];
+        if constexpr (kCol)
+          reinterpret_cast<uint4*>(args.sf_col + (tile_x * row_tiles128 + tile_y) * 512)[lane] =
+              reinterpret_cast<const uint4*>(sf_col_stage)[lane];
+        __syncwarp();
+        if (lane == 0) {
+          tile_done[sfb] = 0;
+          st_release_shared(&sf_free[sfb], static_cast<uint32_t>((i >> 2) + kSfBufs));
+        }
+      }
+    }
+  }
+}
+
+template <bool kRow, bool kCol, bool kFp8, bool kHadRow, bool kHadCol>
+cudaError_t launch_cast_t(const CUtensorMap& tm, const CastArgs& args, int col_tiles, int row_tiles128,
+                          int num_tiles, int dev, cudaStream_t stream) {
+  auto kernel = cast_kernel<kRow, kCol, kFp8, kHadRow, kHadCol>;
+  static std::atomic<int> ctas[64];  // resident CTAs on the whole GPU, per device
+  int grid = (dev >= 0 && dev < 64) ? ctas[dev].load(std::memory_order_relaxed) : 0;
+  if (grid == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCastSmemBytes);
     if (e != cudaSuccess) return e;
     int occ = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, cast_kernel<kRow, kCol, kFp8>, kThreads,
-                                                      kCastSmemBytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, kCastSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    per_sm = std::max(1, occ) * sms;  // resident CTAs on the whole GPU
-    if (dev >= 0 && dev < 64) ctas_per_sm[dev].store(per_sm, std::memory_order_relaxed);
+    grid = std::max(1, occ) * sms;
+    if (dev >= 0 && dev < 64) ctas[dev].store(grid, std::memory_order_relaxed);
   }
   int* status = device_status_word();
   if (status == nullptr) return cudaErrorUnknown;
   // cudaLaunchKernelEx reports this launch's own error; the thread's last
   // error may hold a stale, unrelated one (e.g. a not-ready query result).
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(std::min(num_tiles, per_sm)), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min(num_tiles, grid)), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kCastSmemBytes;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, cast_kernel<kRow, kCol, kFp8>, tm, args, col_tiles, num_tiles, status);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tm, args, col_tiles, row_tiles128, num_tiles, status);
+}
+
+template <bool kRow, bool kCol, bool kFp8>
+cudaError_t launch_had(const CUtensorMap& tm, const CastArgs& args, int col_tiles, int row_tiles128,
+                       int num_tiles, int dev, cudaStream_t stream) {
+  const bool hr = kRow && (args.flags & kFlagHadamardRow) != 0;
+  const bool hc = kCol && (args.flags & kFlagHadamardCol) != 0;
+  if constexpr (kRow && kCol) {
+    if (hr && hc) return launch_cast_t<true, true, kFp8, true, true>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    if (hr) return launch_cast_t<true, true, kFp8, true, false>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    if (hc) return launch_cast_t<true, true, kFp8, false, true>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    return launch_cast_t<true, true, kFp8, false, false>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+  } else if constexpr (kRow) {
+    if (hr) return launch_cast_t<true, false, kFp8, true, false>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    return launch_cast_t<true, false, kFp8, false, false>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+  } else {
+    if (hc) return launch_cast_t<false, true, kFp8, false, true>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    return launch_cast_t<false, true, kFp8, false, false>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+  }
 }
 
 }  // namespace
@@ -395,7 +478,7 @@ cudaError_t launch_cast(const CastArgs& args, cudaStream_t stream) {
   CUtensorMap tm;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(args.cols), static_cast<cuuint64_t>(args.rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(args.ldx) * 2};
-  cuuint32_t box[2] = {kTile / 2, kTile};  // 64 columns (128 bytes) x 128 rows
+  cuuint32_t box[2] = {kSlabCols / 2, kSlabRows};  // 64 columns (128 bytes) x 32 rows
   cuuint32_t estrides[2] = {1, 1};
   if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(args.x), dims, strides, box,
          estrides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -404,18 +487,22 @@ cudaError_t launch_cast(const CastArgs& args, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int64_t col_tiles = (args.cols + kTile - 1) / kTile;
-  const int64_t row_tiles = (args.rows + kTile - 1) / kTile;
-  if (col_tiles * row_tiles > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
-  const int num_tiles = static_cast<int>(col_tiles * row_tiles);
+  const int64_t col_tiles = (args.cols + kSlabCols - 1) / kSlabCols;
+  const int64_t row_tiles128 = (args.rows + 127) / 128;
+  // whole 128 x 128 tiles: the slabs past the last row only write the zero
+  // scales of the tile padding
+  const int64_t num_tiles = row_tiles128 * col_tiles;
+  if (4 * num_tiles > (int64_t(1) << 31) - 1 || row_tiles128 * 128 > (int64_t(1) << 31) - 1)
+    return cudaErrorInvalidValue;
+  const int ns = static_cast<int>(num_tiles), ct = static_cast<int>(col_tiles), rt = static_cast<int>(row_tiles128);
   const bool row = args.q_row != nullptr, col = args.q_col != nullptr;
   if (args.flags & kFlagFp8) {
     if (row || !col) return cudaErrorInvalidValue;  // MXFP8: column output only
-    return launch_cast_t<false, true, true>(tm, args, int(col_tiles), num_tiles, dev, stream);
+    return launch_had<false, true, true>(tm, args, ct, rt, ns, dev, stream);
   }
-  if (row && col) return launch_cast_t<true, true>(tm, args, int(col_tiles), num_tiles, dev, stream);
-  if (row) return launch_cast_t<true, false>(tm, args, int(col_tiles), num_tiles, dev, stream);
-  if (col) return launch_cast_t<false, true>(tm, args, int(col_tiles), num_tiles, dev, stream);
+  if (row && col) return launch_had<true, true, false>(tm, args, ct, rt, ns, dev, stream);
+  if (row) return launch_had<true, false, false>(tm, args, ct, rt, ns, dev, stream);
+  if (col) return launch_had<false, true, false>(tm, args, ct, rt, ns, dev, stream);
   return cudaSuccess;
 }
 
