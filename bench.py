@@ -80,9 +80,10 @@ def strip_comments(src: str) -> str:
 
 
 def gemm_source_hash():
-    """sha256[:16] of the GEMM's code (gemm.cu + ptx.cuh, comments stripped)."""
+    """sha256[:16] of the GEMM's code (gemm.cu and every header it includes,
+    comments stripped)."""
     h = hashlib.sha256()
-    for f in ("gemm.cu", "ptx.cuh"):
+    for f in ("gemm.cu", "ptx.cuh", "quant.cuh", "internal.h"):
         text = open(os.path.join(ROOT, "quantization_mxfp4_cast_gb300", "csrc", f)).read()
         h.update(strip_comments(text).encode())
     return h.hexdigest()[:16]
@@ -297,6 +298,42 @@ class Step:
         return sum(t.numel() * t.element_size() for t in self.out_host.values())
 
 
+def host_link_rates(step, streams, dev, reps=5):
+    """This box's pinned host<->device copy rates for the step's own tensors:
+    uploads alone, downloads alone, and both directions at once on their two
+    streams (no compute): the floor under the end-to-end leg."""
+    s_in, _, s_out = streams
+    h, xs = step.host, step.e2e_in[0]
+    outs, hout = step.e2e_out[0], step.e2e_host_out[0]
+
+    def up():
+        with torch.cuda.stream(s_in):
+            for dst, src in zip(xs, (h["x"], h["w"], h["dy"])):
+                dst.copy_(src, non_blocking=True)
+
+    def down():
+        with torch.cuda.stream(s_out):
+            for name, src in zip(("y", "dx", "dw"), outs):
+                hout[name].copy_(src, non_blocking=True)
+
+    def timed(fns):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            for f in fns:
+                f()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps
+
+    up(), down()
+    t_up, t_down, t_both = timed([up]), timed([down]), timed([up, down])
+    bi, bo = step.h2d_bytes(), step.d2h_bytes()
+    return {"h2d_gbs": bi / t_up / 1e9, "d2h_gbs": bo / t_down / 1e9,
+            "both_directions_gbs": (bi + bo) / t_both / 1e9, "copy_floor_ms_per_step": t_both * 1e3,
+            "what": "pinned copies of the step's inputs (H2D) and outputs (D2H), alone and both at once; "
+                    "copy_floor_ms_per_step is the time of one step's copies with no compute"}
+
+
 # ----------------------------------------------------------------------------- layer and FP8 legs
 def time_loop(fn, iters, warm, stream):
     """Mean seconds per call of fn() on `stream` (CUDA events, after warm-up)."""
@@ -406,30 +443,42 @@ def time_each(fn, iters, stream, flush):
     return sum(e0.elapsed_time(e1) for e0, e1 in evs) / iters / 1e3
 
 
-def cast_only_leg(m, dev, stream, hbm_gbs, iters=10):
+def cast_only_leg(m, dev, stream, hbm_gbs, iters=20):
     """The cast-only workload: bf16 activations [8192, 4096] ~ N(0,1) with 0.1%
     of the entries scaled by 50; the dual cast (row-wise + transposed) with
-    the Hadamard off and on (both outputs), and the row-wise cast alone."""
-    x = synth.cast_input().to(dev)
-    R, C = x.shape
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    dual = m.mxfp4_cast_dual(x, stream=stream)
-    row = m.mxfp4_cast(x, stream=stream)
+    the Hadamard off and on (both outputs), and the row-wise cast alone.
+    Timed back to back over rotating input/output sets whose total is more
+    than twice the L2, so every launch reads and writes HBM; the isolated time
+    of one launch after an L2 overwrite is reported beside it."""
+    x0 = synth.cast_input().to(dev)
+    R, C = x0.shape
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_set = R * C * (2 + 1.0625)
+    nsets = max(4, int(2 * l2 / per_set) + 1)
+    xs = [x0.clone() for _ in range(nsets)]
+    duals = [m.mxfp4_cast_dual(x, stream=stream) for x in xs]
+    rows = [m.mxfp4_cast(x, stream=stream) for x in xs]
     runs = {
-        "dual": (lambda: m.mxfp4_cast_dual(x, out=dual, stream=stream), 3.0625),
-        "dual_hadamard_row_col": (lambda: m.mxfp4_cast_dual(x, hadamard_row=True, hadamard_col=True, out=dual,
-                                                             stream=stream), 3.0625),
-        "row_only": (lambda: m.mxfp4_cast(x, q=row[0], sf=row[1], stream=stream), 2.53125),
+        "dual": (lambda k: m.mxfp4_cast_dual(xs[k], out=duals[k], stream=stream), 3.0625),
+        "dual_hadamard_row_col": (lambda k: m.mxfp4_cast_dual(xs[k], hadamard_row=True, hadamard_col=True,
+                                                               out=duals[k], stream=stream), 3.0625),
+        "dual_hadamard_col": (lambda k: m.mxfp4_cast_dual(xs[k], hadamard_col=True, out=duals[k], stream=stream),
+                              3.0625),
+        "row_only": (lambda k: m.mxfp4_cast(xs[k], q=rows[k][0], sf=rows[k][1], stream=stream), 2.53125),
     }
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     out = {}
     for name, (fn, bpe) in runs.items():
-        t = time_each(fn, iters, stream, flush)
+        t = time_loop(lambda it=[0]: (fn(it[0] % nsets), it.__setitem__(0, it[0] + 1)), iters, 4, stream)
+        t_iso = time_each(lambda: fn(0), 10, stream, flush)
         gbs = R * C * bpe / t / 1e9
-        out[name] = {"us": t * 1e6, "gbs": gbs, "frac_of_measured_hbm": gbs / hbm_gbs, "frac_of_8tbs": gbs / 8000.0}
-    del flush
+        out[name] = {"us": t * 1e6, "gbs": gbs, "frac_of_measured_hbm": gbs / hbm_gbs, "frac_of_8tbs": gbs / 8000.0,
+                     "isolated_us": t_iso * 1e6, "isolated_gbs": R * C * bpe / t_iso / 1e9}
+    del flush, xs, duals, rows
     return {"shape": [R, C], "bytes_per_element": {"dual": 3.0625, "row_only": 2.53125}, **out,
-            "what": "cast-only workload (activations with 0.1% outliers x50), each launch alone after an "
-                    "L2 overwrite, CUDA events"}
+            "what": f"cast-only workload (activations with 0.1% outliers x50): {iters} launches back to back over "
+                    f"{nsets} rotating input/output sets ({nsets * per_set / 1e6:.0f} MB > 2x L2), CUDA events; "
+                    "isolated_*: one launch alone after an L2 overwrite"}
 
 
 def gemm_shapes_leg(m, dev, stream, iters=10):
@@ -576,6 +625,65 @@ def oracle_sample(rows_cast: int, out_rows: int, out_cols: int, nthreads: int):
     return est, time.perf_counter() - t_all, desc
 
 
+def sample_idx(n, k, seed):
+    """k distinct indices of range(n), the first and last always among them."""
+    rng = np.random.default_rng(seed)
+    idx = rng.choice(n, size=min(k, n), replace=False)
+    idx[:2] = [0, n - 1]
+    return np.unique(idx)
+
+
+def gemm_within_tolerance(got, ref):
+    """|gpu - oracle| <= 2^-8 |oracle| + 1e-3 rms(oracle) elementwise, rms over
+    the sampled oracle values.  Returns (ok, worst excess over the bound)."""
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    excess = np.abs(got - ref) - (2.0 ** -8 * np.abs(ref) + 1e-3 * rms)
+    return bool(np.isfinite(got).all() and (excess <= 0).all()), float(excess.max())
+
+
+def parity_gate(step, nthreads, n_cast=64, n_out=64):
+    """The step's own results against the oracle, before any number is
+    reported: the row and column casts (codes and scales) of the first
+    n_cast rows / columns of X, W and dY, and an n_out x n_out sample of each
+    of Y, dX and dW (at the GEMM tolerance, rms over the sample's 4096 oracle
+    values).  Returns a summary; 'ok' is False on any mismatch."""
+    import oracle
+    bx, bw, bdy = oracle_inputs()
+    out = {"casts": {}, "gemms": {}}
+    ok = True
+    for name, arr, q, had in (("X", bx, step.qx, True), ("W", bw, step.qw, False), ("dY", bdy, step.qdy, True)):
+        R, C = arr.shape
+        cr, sr = oracle.cast_rows(np.ascontiguousarray(arr[:n_cast]))
+        cc, sc = oracle.cast_cols(np.ascontiguousarray(arr[:, :n_cast]), hadamard=had)
+        got_sr = oracle.sf_tile_to_linear(q[1].cpu().numpy(), R, C // 32)[:n_cast]
+        got_sc = oracle.sf_tile_to_linear(q[3].cpu().numpy(), C, R // 32)[:n_cast]
+        same = (np.array_equal(q[0][:n_cast].cpu().numpy(), cr) and np.array_equal(got_sr, sr)
+                and np.array_equal(q[2][:n_cast].cpu().numpy(), cc) and np.array_equal(got_sc, sc))
+        out["casts"][name] = "bit-exact" if same else "MISMATCH"
+        ok &= same
+    si, sj = sample_idx(M, n_out, 11), sample_idx(N, n_out, 12)
+    sk, sn = sample_idx(K, n_out, 13), sample_idx(N, n_out, 14)
+    cases = {
+        "Y": (step.y, si, sj, oracle.cast_rows(np.ascontiguousarray(bx[si])),
+              oracle.cast_rows(np.ascontiguousarray(bw[sj]))),
+        "dX": (step.dx, si, sk, oracle.cast_rows(np.ascontiguousarray(bdy[si])),
+               oracle.cast_cols(np.ascontiguousarray(bw[:, sk]))),
+        "dW": (step.dw, sn, sk, oracle.cast_cols(np.ascontiguousarray(bdy[:, sn]), hadamard=True),
+               oracle.cast_cols(np.ascontiguousarray(bx[:, sk]), hadamard=True)),
+    }
+    for name, (c, ri, ci, (ca, sa), (cb, sb)) in cases.items():
+        ref = oracle.gemm_mxfp4(ca, sa, cb, sb, nthreads=nthreads)
+        dev = c.device
+        got = c[torch.from_numpy(ri).to(dev)][:, torch.from_numpy(ci).to(dev)].float().cpu().numpy().astype(np.float64)
+        good, excess = gemm_within_tolerance(got, ref)
+        out["gemms"][name] = {"ok": good, "worst_excess": excess, "samples": int(ref.size)}
+        ok &= good
+    out["ok"] = bool(ok)
+    out["what"] = (f"before timing: casts of the first {n_cast} rows and columns of X, W, dY bit-exact against the "
+                   f"oracle; {n_out}x{n_out} sampled outputs of Y, dX, dW within 2^-8|ref| + 1e-3 rms(ref)")
+    return out
+
+
 def cpu_threads():
     try:
         return len(os.sched_getaffinity(0))
@@ -612,6 +720,12 @@ def max_over_ranks(v, world, dev):
     return float(t.item())
 
 
+def bench_config(world):
+    """The workload description both arms print."""
+    return {"workload": WORKLOAD, "M": M, "N": N, "K": K, "parallelism": f"replicas x{world}",
+            "l2": "no flush: the step streams ~1.1 GB through HBM per iteration (inputs larger than the 129 MB L2)"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
@@ -633,9 +747,12 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle; fp32 Hadamard)", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K},
+            "config": bench_config(world),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
                              "sample": desc},
+            "timing": {"ms_per_step": "median over the timed steps of the per-step estimate: each step times a "
+                                      "bounded sample of the workload and extrapolates it linearly to one full "
+                                      "step, so ms_per_step is far longer than the run's wall time"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -677,6 +794,11 @@ def main():
     stream.synchronize()
     if m.device_status() != 0:
         raise RuntimeError("device status word set during warm-up")
+    # the warm-up steps' outputs against the oracle: no number without parity
+    parity = parity_gate(step, cpu_threads())
+    if not parity["ok"]:
+        log("parity gate FAILED: " + json.dumps(parity))
+        return 3
 
     # --------------------------------------------------------------- timed region (HBM-resident inputs)
     # One step (6 launches through the C ABI) is captured once as a CUDA graph
@@ -782,10 +904,13 @@ def main():
         torch.cuda.synchronize()
         barrier(world)
         t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+        link = host_link_rates(step, streams, dev)
+        ms_e2e = t_e2e / k_e2e * 1e3
         e2e = {"value": world * STEP_FLOPS * k_e2e / t_e2e / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": step.h2d_bytes(), "d2h_bytes_per_step": step.d2h_bytes(),
-               "steps": k_e2e, "ms_per_step": t_e2e / k_e2e * 1e3,
-               "pipeline": "double-buffered: upload of step i+1 and download of step i-1 overlap step i's compute"}
+               "steps": k_e2e, "ms_per_step": ms_e2e,
+               "pipeline": "double-buffered: upload of step i+1 and download of step i-1 overlap step i's compute",
+               "host_link": link, "frac_of_copy_floor": link["copy_floor_ms_per_step"] / ms_e2e}
 
     extra = {}
     if not args.no_extra:
@@ -812,13 +937,13 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "mxfp4 (e2m1 x e2m1, e8m0 scales) -> f32 accum -> bf16",
             "data": "synthetic (seeded N(0,sigma) bf16: X,W ~ N(0,0.02), dY ~ N(0,1e-3))",
-            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "parallelism": f"replicas x{world}",
-                       "l2": "no flush: the step streams ~1.1 GB through HBM per iteration (inputs larger than the 129 MB L2)"},
+            "config": bench_config(world),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
                          "frac": achieved / fp4_peak, "traffic": traffic,
                          "kernel": "gemm_mxf4_kernel (mean of the fwd/dgrad/wgrad launches)",
                          "peak_source": f"{peaks['source']} bf16 burst {peaks['bf16']:.1f} TFLOP/s x nominal "
                                         f"dense fp4/bf16 ratio {NOMINAL_FP4_OVER_BF16:.0f}"},
+            "parity": parity,
             "breakdown": breakdown,
             "cpu_baseline": cpu,
             **({"extra": extra} if extra else {}),

@@ -233,26 +233,35 @@ mxfp4_status gemm_fp4_bf16_wgrad(const uint16_t* dy, const uint16_t* x, uint16_t
 mxfp4_status mxfp4_device_status(int reset, int* out_status);
 
 /* Size of the library-owned device scratch array used by
- * gemm_fp4_bf16_fwd_noalloc (32 MiB; held on every GPU that loads the
- * library, until the process exits). */
+ * gemm_fp4_bf16_fwd_noalloc (32 MiB; taken on a device by the first call
+ * there, held until the process exits). */
 #define MXFP4_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 
 /*
  * gemm_fp4_bf16_fwd_noalloc -- the same operation as gemm_fp4_bf16_fwd
  * (Y[M,N] = X[M,K] . W[N,K]^T through MXFP4, bf16 in/out) for callers that
- * cannot allocate device memory: code running where CUDA allocation calls are
- * not allowed, or a plugin that owns no device memory beyond its inputs and
- * outputs.  It takes no workspace; the quantized X and W go to a file-scope
- * device array of MXFP4_NOALLOC_SCRATCH_BYTES inside the library.  The pages
- * have no counterpart to this entry point: it exists for those callers only.
- *   Requires mxfp4_workspace_bytes(MXFP4_OP_FWD, M, N, K) <=
- *   MXFP4_NOALLOC_SCRATCH_BYTES, else returns MXFP4_ERR_WORKSPACE and launches
- *   nothing.  Other arguments and errors as gemm_fp4_bf16_fwd.
- *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *   The first call on each device (with that device current) looks up the
- *   array's device address once; make that first call before any stream
- *   capture.  All calls share the one array: calls whose work overlaps on the
- *   GPU (other streams, other host threads) race on it.
+ * cannot allocate device memory: a plugin whose device memory all belongs to
+ * the host framework's allocator and which is handed only its inputs and
+ * outputs, or code that must not make allocating CUDA calls where it runs.
+ * It takes no workspace; the quantized X and W go to a file-scope device
+ * array of MXFP4_NOALLOC_SCRATCH_BYTES inside the library.  The pages have no
+ * counterpart to this entry point: it exists for those callers only.
+ *   Arguments: checked as gemm_fp4_bf16_fwd checks them, in the same order
+ *   and with the same errors; M == 0 or N == 0 is a no-op.  Then
+ *   mxfp4_workspace_bytes(MXFP4_OP_FWD, M, N, K) must not exceed
+ *   MXFP4_NOALLOC_SCRATCH_BYTES, else MXFP4_ERR_WORKSPACE and nothing is
+ *   launched.
+ *   First call on a device: CUDA loads the library's device code lazily, so
+ *   the first call on each device loads the array -- the one moment its
+ *   32 MiB of device memory is taken.  That call fails with MXFP4_ERR_CUDA
+ *   (cudaErrorMemoryAllocation in mxfp4_last_cuda_error) if the device is
+ *   full: make it before the host framework reserves its memory pool, and
+ *   before any stream capture.  It also looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it.  Later
+ *   calls allocate nothing: no cudaMalloc, cudaFree or allocating library
+ *   call.
+ *   All calls share the one array: calls whose work overlaps on the GPU
+ *   (other streams, other host threads) race on it.
  */
 mxfp4_status gemm_fp4_bf16_fwd_noalloc(const uint16_t* x, const uint16_t* w, uint16_t* y,
                                        int64_t M, int64_t N, int64_t K, void* stream);

@@ -34,6 +34,8 @@ mxfp4_status from_cuda(cudaError_t e) {
 
 }  // namespace
 
+int mxfp4::status_from_cuda(cudaError_t e) { return from_cuda(e); }
+
 // This library links its own CUDA runtime, whose per-thread current device is
 // separate from the caller's (torch's) runtime: a thread that torch created
 // (an autograd worker, say) may have no current context here at all, and
@@ -98,6 +100,22 @@ mxfp4_status check_out(const void* p) {
   if (!aligned16(p)) return MXFP4_ERR_MISALIGNED;
   return MXFP4_OK;
 }
+
+}  // namespace
+
+// The argument checks of gemm_fp4_bf16_fwd before its workspace check, in its
+// order; MXFP4_OK for M == 0 or N == 0 (nothing to do).
+int mxfp4::check_fwd_args(const uint16_t* x, const uint16_t* w, const uint16_t* y, int64_t M, int64_t N,
+                          int64_t K) {
+  mxfp4_status st = check_bf16_in(x, M, K, K);
+  if (st == MXFP4_OK) st = check_bf16_in(w, N, K, K);
+  if (st != MXFP4_OK || M == 0 || N == 0) return st;
+  st = check_out(y);
+  if (st == MXFP4_OK && N % 8 != 0) st = MXFP4_ERR_MISALIGNED;
+  return st;
+}
+
+namespace {
 
 #define MXFP4_TRY(expr)                      \
   do {                                       \
@@ -341,11 +359,8 @@ size_t mxfp4_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
 
 mxfp4_status gemm_fp4_bf16_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y, int64_t M,
                                int64_t N, int64_t K, void* ws, size_t ws_bytes, void* stream) {
-  MXFP4_TRY(check_bf16_in(x, M, K, K));
-  MXFP4_TRY(check_bf16_in(w, N, K, K));
+  MXFP4_TRY(static_cast<mxfp4_status>(mxfp4::check_fwd_args(x, w, y, M, N, K)));
   if (M == 0 || N == 0) return MXFP4_OK;
-  MXFP4_TRY(check_out(y));
-  if (N % 8 != 0) return MXFP4_ERR_MISALIGNED;
   if (ws == nullptr || ws_bytes < mxfp4_workspace_bytes(MXFP4_OP_FWD, M, N, K) || !aligned16(ws))
     return MXFP4_ERR_WORKSPACE;
   MXFP4_TRY(check_device(y));

@@ -710,8 +710,13 @@ cudaError_t launch_gemm_fmt(const GemmArgs& args, cudaStream_t stream, const Cas
   p.num_nt = static_cast<int>((args.N + kBN - 1) / kBN);
   p.num_kt = static_cast<int>((args.K + F::kBK - 1) / F::kBK);
   p.ktiles128 = static_cast<int>(ktiles128);
-  p.group_m = 1;  // powers of two up to 64 while the A panel stays within the budget
-  while (p.group_m < 64 && 2 * p.group_m * kBM * row_bytes <= kRasterPanelBytes) p.group_m *= 2;
+  // Raster group: powers of two up to 64 row tiles while the group's A panel,
+  // counted in FP4 bytes (K / 2 per row), stays within the budget.  An MXFP8
+  // panel of the same K is twice the bytes and still fits the L2; sizing it
+  // by its own bytes halved the group and streamed B twice (measured on the
+  // wgrad of the 8B down projection: 1.8x the operand bytes read from DRAM).
+  p.group_m = 1;
+  while (p.group_m < 64 && 2 * p.group_m * kBM * (args.K / 2) <= kRasterPanelBytes) p.group_m *= 2;
   p.sf_row = kCastOut ? out->sf_row : nullptr;
   p.sf_col = kCastOut ? out->sf_col : nullptr;
   p.cast_flags = kCastOut ? out->flags : 0u;

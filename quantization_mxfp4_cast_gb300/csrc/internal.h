@@ -71,6 +71,14 @@ int* device_status_word();
 // Reads (and optionally clears) the device status word.  Synchronous.
 cudaError_t read_device_status(int* value, bool reset);
 
+// Records e as the calling thread's last CUDA error (mxfp4_last_cuda_error)
+// and returns the matching status: MXFP4_OK or MXFP4_ERR_CUDA.
+int status_from_cuda(cudaError_t e);
+
+// The argument checks gemm_fp4_bf16_fwd runs before its workspace check, in
+// the same order; MXFP4_OK also when M == 0 or N == 0 (nothing to launch).
+int check_fwd_args(const uint16_t* x, const uint16_t* w, const uint16_t* y, int64_t M, int64_t N, int64_t K);
+
 // Zero-fill of a bf16 matrix (used when K == 0).
 cudaError_t launch_fill_zero_bf16(uint16_t* c, int64_t M, int64_t N, int64_t ldc,
                                   cudaStream_t stream);

@@ -25,14 +25,15 @@ from dataclasses import dataclass
 
 import torch
 
-from . import gemm_fp4, gemm_fp4_cast_out, mxfp4_cast_dual, scales_bytes
+from . import gemm_fp4, gemm_fp4_cast_out, mxfp4_cast, mxfp4_cast_dual, scales_bytes
 
 
 @dataclass
 class MXFP4Tensor:
-    """Both MXFP4 copies of a bf16 matrix T[R, C]: row-wise (codes [R, C/2],
+    """The MXFP4 copies of a bf16 matrix T[R, C]: row-wise (codes [R, C/2],
     blocks of 32 along C) and column-wise (codes [C, R/2], blocks of 32 along
-    R, i.e. T^T quantized), with their tile-layout scales."""
+    R, i.e. T^T quantized), with their tile-layout scales.  The column copy is
+    None when only the row copy was made (a forward with no backward)."""
     rows: int
     cols: int
     q_row: torch.Tensor
@@ -71,6 +72,15 @@ class MXFP4Quantizer:
     def for_grad(cls) -> "MXFP4Quantizer":
         """dY[M, N]: row copy for dgrad, column copy (Hadamard along M) for wgrad."""
         return cls("grad", hadamard_col=True)
+
+    def quantize_rows(self, t: torch.Tensor) -> MXFP4Tensor:
+        """Only the row copy of the 2-D bf16 t (what a forward GEMM reads):
+        one row-wise cast, no transposed copy."""
+        if t.dim() != 2:
+            raise ValueError("quantize_rows expects a 2-D tensor")
+        R, C = t.shape
+        q, sf = mxfp4_cast(t, stream=torch.cuda.current_stream(t.device))
+        return MXFP4Tensor(R, C, q, sf, None, None, self.hadamard_col)
 
     def quantize(self, t: torch.Tensor, out: MXFP4Tensor | None = None) -> MXFP4Tensor:
         """One dual cast of the 2-D bf16 t (rows and columns multiples of 32)."""
@@ -123,7 +133,9 @@ class _MXFP4LinearFn(torch.autograd.Function):
     def forward(ctx, x2, w, w_q, act_q, grad_q):
         M, K = x2.shape
         N = w.shape[0]
-        x_q = act_q.quantize(x2)
+        # the column copy of x serves only the wgrad: without a weight gradient
+        # (inference, or a frozen weight) the row-wise cast alone is made
+        x_q = act_q.quantize(x2) if ctx.needs_input_grad[1] else act_q.quantize_rows(x2)
         stream = torch.cuda.current_stream(x2.device)
         y = gemm_fp4(x_q.q_row, x_q.sf_row, w_q.q_row, w_q.sf_row, M, N, K, stream=stream)
         ctx.x_q, ctx.w_q, ctx.grad_q = x_q, w_q, grad_q
@@ -195,13 +207,19 @@ class _MXFP4StackFn(torch.autograd.Function):
     def forward(ctx, x2, w_qs, *ws):
         M = x2.shape[0]
         stream = torch.cuda.current_stream(x2.device)
-        x_q = MXFP4Quantizer.for_activation().quantize(x2)
+        # without a backward only the row copies are made (the column copies
+        # serve the wgrads)
+        train = any(ctx.needs_input_grad)
+        act = MXFP4Quantizer.for_activation()
+        x_q = act.quantize(x2) if train else act.quantize_rows(x2)
         acts, y = [], None
         for i, (w, w_q) in enumerate(zip(ws, w_qs)):
             N, K = w.shape
             acts.append(x_q)
             if i + 1 < len(ws):
                 nxt = MXFP4Tensor.empty(M, N, True, x2.device)
+                if not train:
+                    nxt.q_col = nxt.sf_col = None
                 gemm_fp4_cast_out(x_q.q_row, x_q.sf_row, w_q.q_row, w_q.sf_row, M, N, K, hadamard_col=True,
                                   out=(nxt.q_row, nxt.sf_row, nxt.q_col, nxt.sf_col), write_c=False,
                                   stream=stream)

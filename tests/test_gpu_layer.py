@@ -162,3 +162,29 @@ def test_stack_inference_matches_training_forward(L):
         y_infer = stack(x)
     torch.cuda.synchronize()
     assert torch.equal(y_train.detach(), y_infer)
+
+
+def test_forward_without_backward_makes_the_row_copy_only(L):
+    # Without a weight gradient the activation's column copy (read only by the
+    # wgrad) is not made: the row-only cast gives the dual cast's row bytes,
+    # and the layer's output is the same with and without autograd.
+    M, N, K = 192, 256, 320
+    w = synth.normal_bf16((N, K), 0.02, seed=90).cuda()
+    x = synth.normal_bf16((M, K), 1.0, seed=91).cuda()
+    q = L.MXFP4Quantizer.for_activation()
+    rows, dual = q.quantize_rows(x), q.quantize(x)
+    torch.cuda.synchronize()
+    assert rows.q_col is None and rows.sf_col is None
+    assert torch.equal(rows.q_row, dual.q_row) and torch.equal(rows.sf_row, dual.sf_row)
+    layer = L.MXFP4Linear(w.clone())
+    y_train = layer(x)
+    with torch.no_grad():
+        y_infer = layer(x)
+    frozen = L.MXFP4Linear(w.clone())
+    frozen.weight.requires_grad_(False)
+    xg = x.clone().requires_grad_(True)
+    y_frozen = frozen(xg)               # dgrad still possible: no wgrad, no column copy of x
+    y_frozen.backward(torch.ones_like(y_frozen))
+    torch.cuda.synchronize()
+    assert torch.equal(y_train.detach(), y_infer) and torch.equal(y_infer, y_frozen.detach())
+    assert xg.grad is not None and torch.isfinite(xg.grad.float()).all()
