@@ -232,6 +232,22 @@ mxfp4_status gemm_fp4_bf16_wgrad(const uint16_t* dy, const uint16_t* x, uint16_t
  */
 mxfp4_status mxfp4_device_status(int reset, int* out_status);
 
+/*
+ * mxfp4_selftest_wait_timeout -- a self-test of the GEMM's bounded waits, for
+ * tests and diagnostics (not part of any computation; the pages have no
+ * counterpart).  Launches gemm_fp4's kernel on the given operands with every
+ * pipeline wait limited to wait_limit_ns (1 ms .. 2 s; the product launches
+ * use 2 s) and the first "stage ready" signal of the first tile withheld, so
+ * that the tensor-core warp's wait runs out: the kernel records
+ * MXFP4_ERR_TIMEOUT in the device status word (mxfp4_device_status), lets its
+ * loads and tensor-core operations in flight complete, and ends; C is left
+ * unwritten or partly written.  No fault, trap or hang is involved and the
+ * context stays usable.  Arguments as gemm_fp4 (M, N, K > 0).
+ */
+mxfp4_status mxfp4_selftest_wait_timeout(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
+                                         const uint8_t* b_sf, uint16_t* c, int64_t M, int64_t N, int64_t K,
+                                         int64_t ldc, uint64_t wait_limit_ns, void* stream);
+
 /* Size of the library-owned device scratch array used by
  * gemm_fp4_bf16_fwd_noalloc (32 MiB; taken on a device by the first call
  * there, held until the process exits). */

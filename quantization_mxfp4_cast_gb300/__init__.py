@@ -36,6 +36,7 @@ ABI_SYMBOLS = (
     "gemm_fp4_bf16_fwd", "gemm_fp4_bf16_dgrad", "gemm_fp4_bf16_wgrad", "mxfp4_device_status",
     "gemm_fp4_bf16_fwd_noalloc", "mxfp4_last_cuda_error", "mxfp4_cuda_error_string",
     "mxfp8_cast_cols", "gemm_mxfp8", "gemm_fp8_bf16_wgrad", "gemm_fp4_cast_out",
+    "mxfp4_selftest_wait_timeout",
 )
 
 _lib = None
@@ -84,6 +85,7 @@ def lib() -> ctypes.CDLL:
                 "gemm_fp8_bf16_wgrad": (I, [P, P, P, I64, I64, I64, U32, P, SZ, P]),
                 "mxfp4_cuda_error_string": (ctypes.c_char_p, [I]),
                 "gemm_fp4_cast_out": (I, [P, P, P, P, P, I64, I64, I64, I64, P, P, P, P, U32, P]),
+                "mxfp4_selftest_wait_timeout": (I, [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_uint64, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -327,6 +329,18 @@ def gemm_fp4_bf16_fwd_noalloc(x, w, y=None, stream=None):
     _check(lib().gemm_fp4_bf16_fwd_noalloc(_ptr(x), _ptr(w), _ptr(y), M, N, K, _stream(stream)),
            "gemm_fp4_bf16_fwd_noalloc")
     return y
+
+
+def selftest_wait_timeout(a, a_sf, b, b_sf, M: int, N: int, K: int, c, wait_limit_ms: float = 20.0,
+                          stream=None) -> None:
+    """Run gemm_fp4's kernel with its first pipeline signal withheld and every
+    wait limited to wait_limit_ms, so that a wait runs out on purpose: the
+    kernel records MXFP4_ERR_TIMEOUT (read it with device_status()) and ends
+    cleanly.  For tests of the failure path only; C is not a result."""
+    _need_cuda(a, a_sf, b, b_sf, c)
+    _check(lib().mxfp4_selftest_wait_timeout(_ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), _ptr(c), M, N, K,
+                                             c.stride(0), int(wait_limit_ms * 1e6), _stream(stream)),
+           "mxfp4_selftest_wait_timeout")
 
 
 def device_status(reset: bool = True) -> int:

@@ -420,6 +420,25 @@ mxfp4_status gemm_fp4_bf16_wgrad(const uint16_t* dy, const uint16_t* x, uint16_t
   return gemm_checked(qdyt.q, qdyt.sf, qxt.q, qxt.sf, dw, N, K, M, K, s);
 }
 
+mxfp4_status mxfp4_selftest_wait_timeout(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
+                                         const uint8_t* b_sf, uint16_t* c, int64_t M, int64_t N, int64_t K,
+                                         int64_t ldc, uint64_t wait_limit_ns, void* stream) {
+  if (wait_limit_ns < 1000000ull || wait_limit_ns > 2000000000ull) return MXFP4_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return MXFP4_ERR_INVALID_ARG;
+  if (K % 32 != 0 || ldc < N) return MXFP4_ERR_INVALID_ARG;
+  MXFP4_TRY(check_out(c));
+  if (ldc % 8 != 0) return MXFP4_ERR_MISALIGNED;
+  MXFP4_TRY(check_out(a));
+  MXFP4_TRY(check_out(a_sf));
+  MXFP4_TRY(check_out(b));
+  MXFP4_TRY(check_out(b_sf));
+  MXFP4_TRY(check_device(c));
+  GemmArgs g{a, a_sf, b, b_sf, c, M, N, K, ldc};
+  const cudaError_t e = mxfp4::launch_gemm_selftest_timeout(g, wait_limit_ns, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidValue) return MXFP4_ERR_INVALID_ARG;
+  return from_cuda(e);
+}
+
 mxfp4_status mxfp4_device_status(int reset, int* out_status) {
   if (out_status == nullptr) return MXFP4_ERR_INVALID_ARG;
   int v = 0;

@@ -114,7 +114,7 @@ struct Fmt {
   static constexpr int kRingBytes = kStages * static_cast<int>(kStageBytes);
   // epilogue staging per warp: the bf16 C block, plus row and column codes
   static constexpr int kEpiBytes = kEpiWarps * kOutStageBytes * (kCastOut ? 3 : 1);
-  static constexpr int kBarrierBytes = (3 * kStages + 2) * 8 + 16;
+  static constexpr int kBarrierBytes = (3 * kStages + 3) * 8 + 16;
   static constexpr uint32_t kSmemSlack = kSmemBytes - (kRingBytes + kEpiBytes + kBarrierBytes);
   // Instruction descriptor: A and B types (kind::mxf4: E2M1 = 1;
   // kind::mxf8f6f4: E4M3 = 0) at bits 7 and 10, both K-major, fp32
@@ -160,6 +160,12 @@ struct PairGemmParams {
   uint8_t* sf_col;
   uint32_t cast_flags;
   int m_tiles128, n_tiles128;
+  // time without progress after which a pipeline wait gives up (2 s), and the
+  // self-test knob: when set, the scale stagers withhold their "stage ready"
+  // signal for the first stage of the first tile, so the MMA warp's wait runs
+  // out (mxfp4_selftest_wait_timeout); 0 on every product launch
+  unsigned long long wait_limit_ns;
+  int withhold_first_scale_signal;
 };
 
 template <bool kFp8, bool kCastOut>
@@ -197,7 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sf_ready = empty + kStages;
   uint64_t* acc_full = sf_ready + kStages;
   uint64_t* acc_empty = acc_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  uint64_t* mma_drain = acc_empty + 1;  // leader: every MMA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -215,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * kEpiWarps);
+    mbar_init(mma_drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -246,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
+      int issued = 0;  // stage loads issued so far
       for (int t = pair; ok && t < num_tiles; t += num_pairs) {
         int mt, nt;
         tile_coords(t, p.num_mt, p.num_nt, p.group_m, mt, nt);
@@ -253,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b_row = nt * kBN + static_cast<int>(rank) * kRowsPerCta;
         const int a_rt = a_row / 128;  // this CTA's scale row tile of A
         for (int kt = 0; kt < p.num_kt; ++kt) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_device_status)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_device_status, p.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -266,11 +275,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           // both 128-row scale tiles of B in one box (measured: 4-7% faster
           // than two 2-D loads)
           tma_load_3d(sSfb + stage * kSfbStage, &tmSfb, &full[stage], 0, kg0 * 4, nt * 2);
+          ++issued;
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
+      }
+      // Every load issued has landed before the CTA may end: the stagers wait
+      // for all of them unless a wait gave up.  The last load into a stage
+      // completes the phase its index gives; nothing follows it.
+      volatile int keep_waiting = 0;  // not the CTA's abort flag: this wait must run its course
+      for (int s = 0; s < kStages && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / kStages) * kStages;
+        mbar_wait(&full[s], (last / kStages) & 1, &keep_waiting, &g_device_status, p.wait_limit_ns);
       }
     }
   } else if (warp == 1) {
@@ -289,11 +307,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int last_nks = static_cast<int>(
           (args.K - static_cast<int64_t>(p.num_kt - 1) * F::kBK + F::kMmaK - 1) / F::kMmaK);
       for (int t = pair; ok && t < num_tiles; t += num_pairs) {
-        ok = mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, &g_device_status);
+        ok = mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, &g_device_status, p.wait_limit_ns);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
         tc_fence_after();
         for (int kt = 0; kt < p.num_kt; ++kt) {
-          ok = mbar_wait(&sf_ready[stage], phase, abort_flag, &g_device_status);
+          ok = mbar_wait(&sf_ready[stage], phase, abort_flag, &g_device_status, p.wait_limit_ns);
           if (!__all_sync(0xFFFFFFFFu, ok)) {
             ok = false;
             break;
@@ -334,6 +352,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         acc_phase ^= 1u;
       }
+      // Every MMA issued (they read both CTAs' shared memory and write their
+      // tensor memory) has completed before the teardown: already so on the
+      // normal path, not when a wait gave up mid-tile.
+      if (elect_one_sync()) tc_commit_pair(mma_drain, 0x1);
+      __syncwarp();
+      volatile int keep_waiting = 0;
+      mbar_wait(mma_drain, 0, &keep_waiting, &g_device_status, p.wait_limit_ns);
+      tc_fence_after();
     }
   } else if (warp < kFirstEpiWarp) {
     // ------------------------------------------------------------ scale stagers (both CTAs)
@@ -348,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int t = pair; ok && t < num_tiles; t += num_pairs) {
       for (int kt = 0; kt < p.num_kt; ++kt) {
-        if (!mbar_wait(&full[stage], phase, abort_flag, &g_device_status)) {
+        if (!mbar_wait(&full[stage], phase, abort_flag, &g_device_status, p.wait_limit_ns)) {
           ok = false;
           break;
         }
@@ -372,7 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(leader_ready0 + stage * 8u);  // the issuing CTA's barrier
+        const bool withhold = p.withhold_first_scale_signal && t == pair && kt == 0;
+        if (lane == 0 && !withhold) mbar_arrive_cluster(leader_ready0 + stage * 8u);  // the issuing CTA's barrier
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
@@ -398,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = pair; t < num_tiles; t += num_pairs) {
       int mt, nt;
       tile_coords(t, p.num_mt, p.num_nt, p.group_m, mt, nt);
-      if (!mbar_wait(acc_full, acc_phase, abort_flag, &g_device_status)) break;
+      if (!mbar_wait(acc_full, acc_phase, abort_flag, &g_device_status, p.wait_limit_ns)) break;
       tc_fence_after();
       // Read all 128 columns (4 x 32) as bf16 pairs, then release the accumulator.
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + h * 128;
@@ -662,7 +689,8 @@ cudaError_t launch_fill_zero_bf16(uint16_t* c, int64_t M, int64_t N, int64_t ldc
 namespace {
 
 template <bool kFp8, bool kCastOut = false>
-cudaError_t launch_gemm_fmt(const GemmArgs& args, cudaStream_t stream, const CastOutArgs* out = nullptr) {
+cudaError_t launch_gemm_fmt(const GemmArgs& args, cudaStream_t stream, const CastOutArgs* out = nullptr,
+                            unsigned long long wait_limit_ns = kWaitLimitNs, bool withhold = false) {
   using F = Fmt<kFp8, kCastOut>;
   if (args.M == 0 || args.N == 0) return cudaSuccess;
   if (args.K == 0) {  // C = 0, and its casts are those of a zero matrix: all bytes 0x00
@@ -722,6 +750,8 @@ cudaError_t launch_gemm_fmt(const GemmArgs& args, cudaStream_t stream, const Cas
   p.cast_flags = kCastOut ? out->flags : 0u;
   p.m_tiles128 = static_cast<int>((args.M + 127) / 128);
   p.n_tiles128 = static_cast<int>((args.N + 127) / 128);
+  p.wait_limit_ns = wait_limit_ns;
+  p.withhold_first_scale_signal = withhold ? 1 : 0;
   const int64_t tiles = static_cast<int64_t>(p.num_mt) * p.num_nt;
   const int pairs = static_cast<int>(std::min<int64_t>(tiles, max_pairs<kFp8, kCastOut>(dev)));
 
@@ -752,6 +782,11 @@ cudaError_t launch_gemm_mxfp8(const GemmArgs& args, cudaStream_t stream) {
 
 cudaError_t launch_gemm_cast_out(const GemmArgs& args, const CastOutArgs& out, cudaStream_t stream) {
   return launch_gemm_fmt<false, true>(args, stream, &out);
+}
+
+cudaError_t launch_gemm_selftest_timeout(const GemmArgs& args, unsigned long long wait_limit_ns,
+                                         cudaStream_t stream) {
+  return launch_gemm_fmt<false>(args, stream, nullptr, wait_limit_ns, true);
 }
 
 }  // namespace mxfp4

@@ -52,6 +52,12 @@ struct CastOutArgs {
 // Requires M % 32 == 0 and N % 32 == 0.  args.c may be null (no bf16 C is
 // written) when at least one cast output is given.
 cudaError_t launch_gemm_cast_out(const GemmArgs& args, const CastOutArgs& out, cudaStream_t stream);
+// Self-test of the bounded waits: the MXFP4 GEMM with the given wait limit and
+// its first "stage ready" signal withheld, so that a wait runs out, the
+// kernel records MXFP4_ERR_TIMEOUT in the status word and every role leaves
+// (after its loads and MMAs in flight have completed).  C is not written.
+cudaError_t launch_gemm_selftest_timeout(const GemmArgs& args, unsigned long long wait_limit_ns,
+                                         cudaStream_t stream);
 // The same GEMM on MXFP8 (E4M3) operands: codes [rows, K] bytes, same scale layout.
 cudaError_t launch_gemm_mxfp8(const GemmArgs& args, cudaStream_t stream);
 

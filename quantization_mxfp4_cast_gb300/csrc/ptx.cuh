@@ -66,9 +66,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete.  `abort_flag` (shared
 // memory) lets the other roles of the CTA stop waiting once one role gave up;
 // `status_word` (global memory) receives MXFP4_ERR_TIMEOUT on a time-out.
+// `limit_ns` is the time without progress after which the wait gives up.
 template <bool kClusterScope = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag, int* status_word) {
+                                          volatile int* abort_flag, int* status_word,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait<kClusterScope>(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   uint32_t spins = 0;
@@ -76,7 +78,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     if (mbar_try_wait<kClusterScope>(bar, parity)) return true;
     if ((++spins & 63u) == 0) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicExch(status_word, 6 /* MXFP4_ERR_TIMEOUT */);
         return false;
