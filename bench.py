@@ -330,6 +330,8 @@ def host_link_rates(step, streams, dev, reps=5):
     bi, bo = step.h2d_bytes(), step.d2h_bytes()
     return {"h2d_gbs": bi / t_up / 1e9, "d2h_gbs": bo / t_down / 1e9,
             "both_directions_gbs": (bi + bo) / t_both / 1e9, "copy_floor_ms_per_step": t_both * 1e3,
+            "upload_ms": t_up * 1e3, "download_ms": t_down * 1e3,
+            "cuda_device_max_connections": os.environ.get("CUDA_DEVICE_MAX_CONNECTIONS", "unset (8)"),
             "what": "pinned copies of the step's inputs (H2D) and outputs (D2H), alone and both at once; "
                     "copy_floor_ms_per_step is the time of one step's copies with no compute"}
 
@@ -910,7 +912,11 @@ def main():
                "h2d_bytes_per_step": step.h2d_bytes(), "d2h_bytes_per_step": step.d2h_bytes(),
                "steps": k_e2e, "ms_per_step": ms_e2e,
                "pipeline": "double-buffered: upload of step i+1 and download of step i-1 overlap step i's compute",
-               "host_link": link, "frac_of_copy_floor": link["copy_floor_ms_per_step"] / ms_e2e}
+               "host_link": link, "frac_of_copy_floor": link["copy_floor_ms_per_step"] / ms_e2e,
+               "serialized_ms_per_step": link["upload_ms"] + link["download_ms"] + ms_per_step,
+               "reading": "ms_per_step near copy_floor_ms_per_step: uploads, downloads and compute overlap; "
+                          "near serialized_ms_per_step (upload + download + device step): they ran one after "
+                          "another"}
 
     extra = {}
     if not args.no_extra:
