@@ -126,14 +126,17 @@ __device__ __forceinline__ bool wait_word(const uint32_t* p, uint32_t want, vola
   }
 }
 
-// The CTA takes the 128 x 128 tiles t = blockIdx.x + k * gridDim.x (k = 0,
-// 1, ...) of x; tile t covers rows 128 * (t / col_tiles) and columns
-// 128 * (t % col_tiles).  Its local slab i = 4k + j is the tile's 32-row block
-// j, so the four slabs of a tile are handed out one after the other and
-// quantized side by side by four warps: the column codes of a tile's column
-// (four 16-byte pieces) are written together, and its two 512-byte scale
-// tiles are assembled in shared memory and written whole by the warp that
-// finishes the tile's last slab.
+// Tile t of x covers rows 128 * (t / col_tiles) and columns 128 * (t %
+// col_tiles).  With G = gridDim.x, the first floor(num_tiles / G) * G tiles
+// are dealt out whole: the CTA owns tiles t = blockIdx.x + k * G, and its local
+// slab i = 4k + j is tile k's 32-row block j, so the four slabs of a tile are
+// handed out one after the other and quantized side by side by four warps --
+// the column codes of a tile's column (four 16-byte pieces) are written
+// together, and its two 512-byte scale tiles are assembled in shared memory
+// and written whole by the warp that finishes the tile's last slab.  The
+// slabs of the last, partial round of tiles are dealt out one by one over all
+// CTAs (tail slab u goes to CTA u mod G), so that every CTA's work is within
+// one slab of every other's; a tail slab writes its scale bytes directly.
 template <bool kRow, bool kCol, bool kFp8, bool kHadRow, bool kHadCol>
 __global__ void __launch_bounds__(kThreads, 1)
     cast_kernel(const __grid_constant__ CUtensorMap tmX, const CastArgs args, int col_tiles,
@@ -158,23 +161,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int64_t rows = args.rows, cols = args.cols;
   const bool linear = (args.flags & kFlagScaleLinear) != 0;
-  // local slabs of this CTA: four per tile
-  const int n_local =
-      4 * static_cast<int>((static_cast<int64_t>(num_tiles) - blockIdx.x + gridDim.x - 1) / gridDim.x);
+  // local slabs of this CTA: four per whole tile, then its tail slabs
+  const int grid = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
+  const int full_rounds = num_tiles / grid;
+  const int tail_slabs = 4 * (num_tiles - full_rounds * grid);
+  const int n_whole = 4 * full_rounds;
+  const int n_local = n_whole + (cta < tail_slabs ? (tail_slabs - cta + grid - 1) / grid : 0);
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-      seq[s] = kNoSlab;
+  {  // set-up spread over the threads (one thread took ~1 us for it)
+    const int t = threadIdx.x;
+    if (t < kStages) {
+      mbar_init(&full[t], 1);
+      mbar_init(&empty[t], 1);
+      seq[t] = kNoSlab;
+      fence_barrier_init();
+    } else if (t < kStages + kSfBufs) {
+      sf_free[t - kStages] = static_cast<uint32_t>(t - kStages);
+      tile_done[t - kStages] = 0;
+    } else if (t == kStages + kSfBufs) {
+      *counter = 0;
+      *abort_flag = 0;
     }
-    for (int b = 0; b < kSfBufs; ++b) {
-      sf_free[b] = static_cast<uint32_t>(b);
-      tile_done[b] = 0;
-    }
-    *counter = 0;
-    *abort_flag = 0;
-    fence_barrier_init();
   }
   if (threadIdx.x == 32 * kConsumerWarps) tma_prefetch_desc(&tmX);
   __syncthreads();
@@ -193,32 +200,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       int slot = 0;
       uint32_t empty_parity = 1;  // from the second pass on: parity of the slot's previous release
       bool ok = true;
-      for (int i = 0; ok && i < n_local; i += 4) {
-        for (int j = 0; j < 4; ++j) {
-          // the slot's previous slab (i + j - kStages) has been quantized
-          if (i + j >= kStages && !mbar_wait(&empty[slot], empty_parity, abort_flag, status)) {
-            ok = false;
-            break;
+      for (int i = 0; ok && i < n_local; ++i) {
+        const int j = i & 3;
+        int rb, ct;
+        uint32_t tail_bit = 0;
+        if (i < n_whole) {
+          rb = 4 * ty + j;
+          ct = tx;
+          if (j == 3) {
+            tx += step_x;
+            ty += step_y;
+            if (tx >= col_tiles) {
+              tx -= col_tiles;
+              ++ty;
+            }
           }
-          const int rb = 4 * ty + j;
-          slot_rb[slot] = static_cast<uint32_t>(rb);
-          slot_ct[slot] = static_cast<uint32_t>(tx);
-          st_release_shared(&seq[slot], static_cast<uint32_t>(i + j));  // publishes the coordinates too
-          uint8_t* dst = ring + slot * kSlabBytes;
-          mbar_arrive_expect_tx(&full[slot], kSlabBytes);
-          tma_load_2d(dst, &tmX, &full[slot], tx * kSlabCols, rb * kSlabRows);
-          tma_load_2d(dst + kHalfBytes, &tmX, &full[slot], tx * kSlabCols + kSlabCols / 2, rb * kSlabRows);
-          issued = i + j + 1;
-          if (++slot == kStages) {
-            slot = 0;
-            empty_parity ^= 1u;
-          }
+        } else {  // tail slab u of the partial round (a handful per CTA)
+          const int u = cta + (i - n_whole) * grid;
+          const int tile = full_rounds * grid + u / 4;
+          rb = 4 * (tile / col_tiles) + (u & 3);
+          ct = tile % col_tiles;
+          tail_bit = 0x80000000u;
         }
-        tx += step_x;
-        ty += step_y;
-        if (tx >= col_tiles) {
-          tx -= col_tiles;
-          ++ty;
+        // the slot's previous slab (i - kStages) has been quantized
+        if (i >= kStages && !mbar_wait(&empty[slot], empty_parity, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        slot_rb[slot] = static_cast<uint32_t>(rb) | tail_bit;
+        slot_ct[slot] = static_cast<uint32_t>(ct);
+        st_release_shared(&seq[slot], static_cast<uint32_t>(i));  // publishes the coordinates too
+        uint8_t* dst = ring + slot * kSlabBytes;
+        mbar_arrive_expect_tx(&full[slot], kSlabBytes);
+        tma_load_2d(dst, &tmX, &full[slot], ct * kSlabCols, rb * kSlabRows);
+        tma_load_2d(dst + kHalfBytes, &tmX, &full[slot], ct * kSlabCols + kSlabCols / 2, rb * kSlabRows);
+        issued = i + 1;
+        if (++slot == kStages) {
+          slot = 0;
+          empty_parity ^= 1u;
         }
       }
       // Every load issued has landed before the CTA may end (a consumer that
@@ -241,12 +260,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (i >= n_local) break;
     const int slot = i % kStages;
     if (!wait_word(&seq[slot], static_cast<uint32_t>(i), abort_flag, status)) break;
-    const int rb = static_cast<int>(slot_rb[slot]);  // 32-row block (published with seq)
+    const uint32_t rbw = slot_rb[slot];  // 32-row block (published with seq), bit 31: tail slab
+    const int rb = static_cast<int>(rbw & 0x7FFFFFFFu);
     const int ct = static_cast<int>(slot_ct[slot]);
-    const int sfb = (i >> 2) % kSfBufs;                // this tile's scale staging buffer
-    uint8_t* sf_row_stage = sf_stage + sfb * kSfStageBytes;
-    uint8_t* sf_col_stage = sf_row_stage + 512;
-    if (!linear && !wait_word(&sf_free[sfb], static_cast<uint32_t>(i >> 2), abort_flag, status)) break;
+    // scale bytes: staged per whole tile, or straight to the tile layout (tail slab)
+    const bool staged = !linear && (rbw >> 31) == 0;
+    const int sfb = (i >> 2) % kSfBufs;  // the whole tile's staging buffer
+    uint8_t* sf_row_stage = staged ? sf_stage + sfb * kSfStageBytes
+                                   : args.sf_row + (static_cast<size_t>(rb >> 2) * col_tiles + ct) * 512;
+    uint8_t* sf_col_stage = staged ? sf_row_stage + 512
+                                   : args.sf_col + (static_cast<size_t>(ct) * row_tiles128 + (rb >> 2)) * 512;
+    if (staged && !wait_word(&sf_free[sfb], static_cast<uint32_t>(i >> 2), abort_flag, status)) break;
     if (!mbar_wait(&full[slot], (i / kStages) & 1, abort_flag, status)) break;
     const uint8_t* tile = ring + slot * kSlabBytes;
     const int64_t c0 = static_cast<int64_t>(ct) * kSlabCols;
@@ -390,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);  // the slot may be refilled
-    if (!linear) {
+    if (staged) {
       // the warp that finishes the tile's last slab writes its scale tiles
       int done = 0;
       if (lane == 0) {
@@ -438,7 +462,7 @@ cudaError_t launch_cast_t(const CUtensorMap& tm, const CastArgs& args, int col_t
   // cudaLaunchKernelEx reports this launch's own error; the thread's last
   // error may hold a stale, unrelated one (e.g. a not-ready query result).
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(std::min(num_tiles, grid)), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(4 * static_cast<int64_t>(num_tiles), grid)), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kCastSmemBytes;
   cfg.stream = stream;
