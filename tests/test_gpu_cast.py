@@ -138,3 +138,43 @@ def test_pitched_input(m):
     codes, scales = oracle.cast_rows(bf16_bits(view.contiguous()))
     assert np.array_equal(q.cpu().numpy(), codes)
     assert np.array_equal(tile_to_lin(sf, 192, 256), scales)
+
+
+@pytest.mark.parametrize("shape", [(2432, 4096), (1280, 2048), (4096, 512)])
+def test_whole_rounds_and_short_tails(m, shape):
+    # 608 tiles = 4 whole rounds of 152 CTAs (no tail); 160 tiles = one round
+    # and 8 tiles dealt out slab by slab; 128 tiles: every slab a tail slab
+    x = synth.with_outliers(synth.normal_bf16(shape, 1.0, seed=shape[0] + shape[1]), frac=0.01)
+    check_dual(m, x, False, True, linear=False)
+    check_row(m, x, False, linear=False)
+
+
+def test_same_stream_ordering(m):
+    # Casts are launched with programmatic stream serialization: a cast may
+    # begin while the previous kernel in the stream finishes, but must not read
+    # its input or write its outputs before that kernel is done.  (1) a torch
+    # kernel writes x, the cast reads it right after; (2) two casts write the
+    # same outputs back to back: the second's bytes must win everywhere.
+    R, C = 1024, 2048
+    a = synth.normal_bf16((R, C), 1.0, seed=41)
+    b = synth.normal_bf16((R, C), 1e-3, seed=42)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        src = a.cuda()
+        x = torch.empty_like(src)
+        for _ in range(3):
+            torch.mul(src, 1.0, out=x)  # the input is produced by the kernel just before the cast
+        out = m.mxfp4_cast_dual(x, hadamard_col=True, stream=s)
+        xb = b.cuda()
+        for _ in range(4):
+            m.mxfp4_cast_dual(x, hadamard_col=True, out=out, stream=s)
+            m.mxfp4_cast_dual(xb, hadamard_col=True, out=out, stream=s)
+    s.synchronize()
+    cr, srr = oracle.cast_rows(bf16_bits(b))
+    cc, scc = oracle.cast_cols(bf16_bits(b), hadamard=True)
+    assert np.array_equal(out[0].cpu().numpy(), cr) and np.array_equal(out[2].cpu().numpy(), cc)
+    assert np.array_equal(out[1].cpu().numpy(), oracle.sf_linear_to_tile(srr))
+    assert np.array_equal(out[3].cpu().numpy(), oracle.sf_linear_to_tile(scc))
+    q, _ = m.mxfp4_cast(x, stream=s)
+    s.synchronize()
+    assert np.array_equal(q.cpu().numpy(), oracle.cast_rows(bf16_bits(a))[0])
