@@ -182,6 +182,8 @@ int main() {
     run<NVF4_4X, 256>("mxf4nvf4_4x_n256", pairs, stages);
     run<MXF8, 256>("mxf8f6f4_n256", pairs, stages);
     run<BF16, 256>("bf16_n256", pairs, stages);
+    run<MXF4, 224>("mxf4_n224", pairs, stages);
+    run<MXF4, 192>("mxf4_n192", pairs, stages);
     run<MXF4, 128>("mxf4_n128", pairs, stages);
     run<MXF4, 16>("mxf4_n16", pairs, stages);
   }

@@ -3,7 +3,8 @@ MMA-only microbenchmark (tests/mma_ceiling.cu: back-to-back tcgen05.mma, no
 loads) on this GPU.  It pins the attainable kind::mxf4 rate that the GEMM's
 efficiency is quoted against: a 256 x 256 x 64 pair MMA per 128 SM cycles,
 32,768 FLOP/clk/SM, four times the bf16 rate of the same benchmark, with the
-NVFP4 form (mxf4nvf4, 4X scales) no faster, and an N = 16 MMA bounded by the
+NVFP4 form (mxf4nvf4, 4X scales) no faster, the time of an MMA linear in N
+(N = 224, 192, 128 at the same rate), and an N = 16 MMA bounded by the
 ~39-cycle issue floor."""
 import os
 import shutil
@@ -39,5 +40,6 @@ def test_kind_mxf4_ceiling(tmp_path):
         assert abs(res[f"bf16_n256_{pairs}"][1] * 4 / mxf4 - 1) < 0.03          # fp4 = 4 x bf16 here
         assert abs(res[f"mxf8f6f4_n256_{pairs}"][1] * 2 / mxf4 - 1) < 0.03      # fp8 = 2 x bf16
         assert res[f"mxf4nvf4_4x_n256_{pairs}"][1] <= 1.03 * mxf4               # NVFP4 form no faster
-        assert abs(res[f"mxf4_n128_{pairs}"][1] / mxf4 - 1) < 0.03              # N = 128: same rate
+        for n in (224, 192, 128):                                               # time linear in N
+            assert abs(res[f"mxf4_n{n}_{pairs}"][1] / mxf4 - 1) < 0.03
         assert 30 <= res[f"mxf4_n16_{pairs}"][0] <= 60                          # issue-bound floor
