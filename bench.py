@@ -9,9 +9,10 @@ quotes):
                        (column copy with the Hadamard);
   three MXFP4 GEMMs -- fwd Y = X W^T, dgrad dX = dY W, wgrad dW = dY^T X.
 `value` is the step's GEMM TFLOP/s (3 x 2MNK per step over the step time,
-casts included) with inputs resident in HBM (the independent launches of a
-step run on three streams, so one kernel's tail overlaps the next one's start;
---serial-step keeps them on one stream); `e2e` repeats it through the same
+casts included) with inputs resident in HBM.  A step is four launches: the
+three casts side by side on three streams, then the three GEMMs in one
+gemm_fp4_grouped launch (--serial-step puts the casts on one stream,
+--separate-gemms times six launches with three gemm_fp4 instead); `e2e` repeats it through the same
 C-ABI calls with host buffers (pinned H2D of X, W, dY and D2H of Y, dX, dW of
 every step inside the timed region, double-buffered so that one step's uploads
 and downloads overlap its neighbours' compute).  `--impl reference` times the
@@ -89,16 +90,18 @@ def gemm_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
-    taken on the current GEMM source; else None."""
+def profiled_traffic(mode):
+    """DRAM bytes per launch of the timed GEMM form ("grouped": the one
+    grouped launch; "separate": mean of the three gemm_fp4 launches) from the
+    committed ncu summary, if it was taken on the current GEMM source; else None."""
     p = os.path.join(ROOT, "profiles", "gemm_mxf4_llama8b_down_train_step.md")
     try:
         text = open(p).read()
     except OSError:
         return None
     src = re.search(r"gemm source sha256\[:16\]:\s*`?([0-9a-f]{16})", text)
-    tr = re.search(r"dram bytes per launch \(mean of the three GEMMs\):\s*([0-9.eE+]+)", text)
+    key = "grouped launch" if mode == "grouped" else "launch \\(mean of the three GEMMs\\)"
+    tr = re.search(r"dram bytes per " + key + r":\s*([0-9.eE+]+)", text)
     if not src or not tr or src.group(1) != gemm_source_hash():
         return None
     return float(tr.group(1))
@@ -198,6 +201,32 @@ class Step:
             if events is not None:
                 events[i][1].record(stream)
 
+    def gemms_grouped(self, stream, outs=None):
+        """fwd, dgrad and wgrad in one gemm_fp4_grouped launch."""
+        m = self.m
+        y, dx, dw = outs if outs is not None else (self.y, self.dx, self.dw)
+        return m.gemm_fp4_grouped([
+            (self.qx[0], self.qx[1], self.qw[0], self.qw[1], M, N, K, y),
+            (self.qdy[0], self.qdy[1], self.qw[2], self.qw[3], M, K, N, dx),
+            (self.qdy[2], self.qdy[3], self.qx[2], self.qx[3], N, K, M, dw)], stream=stream)
+
+    def run_grouped(self, stream, side=None):
+        """The step as four launches: the casts of X, W and dY (side by side on
+        three streams when `side` is given), then one grouped launch of the
+        three GEMMs once all three casts are done."""
+        if side is None:
+            for _, f in self.launches(stream)[:3]:
+                f()
+        else:
+            s1, s2 = side
+            s1.wait_stream(stream)
+            s2.wait_stream(stream)
+            for _, f in self.launches_streams((stream, s1, s2))[:3]:
+                f()
+            stream.wait_stream(s1)
+            stream.wait_stream(s2)
+        self.gemms_grouped(stream)
+
     def run_concurrent(self, stream, side):
         """The same six launches with the independent ones on three streams:
         the casts of X, W and dY side by side, then fwd (X, W), dgrad (dY, W)
@@ -245,14 +274,11 @@ class Step:
     def launches_on(self, xs, outs, stream):
         m = self.m
         x, w, dy = xs
-        y, dx, dw = outs
         return [
             lambda: m.mxfp4_cast_dual(x, hadamard_col=True, out=self.qx, stream=stream),
             lambda: m.mxfp4_cast_dual(w, out=self.qw, stream=stream),
             lambda: m.mxfp4_cast_dual(dy, hadamard_col=True, out=self.qdy, stream=stream),
-            lambda: m.gemm_fp4(self.qx[0], self.qx[1], self.qw[0], self.qw[1], M, N, K, c=y, stream=stream),
-            lambda: m.gemm_fp4(self.qdy[0], self.qdy[1], self.qw[2], self.qw[3], M, K, N, c=dx, stream=stream),
-            lambda: m.gemm_fp4(self.qdy[2], self.qdy[3], self.qx[2], self.qx[3], N, K, M, c=dw, stream=stream),
+            lambda: self.gemms_grouped(stream, outs),
         ]
 
     def run_e2e_pipelined(self, n_steps, streams, ev):
@@ -771,7 +797,9 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the layer-API leg and the cuBLASLt FP8 reference GEMMs")
     ap.add_argument("--serial-step", action="store_true",
-                    help="capture the six launches on one stream instead of three")
+                    help="capture the step's launches on one stream instead of three")
+    ap.add_argument("--separate-gemms", action="store_true",
+                    help="time the step as six launches (three gemm_fp4) instead of one grouped GEMM launch")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
         log("warmup raised to 3 (minimum)")
@@ -790,9 +818,20 @@ def main():
     step = Step(m, dev)
     torch.cuda.synchronize()
 
+    side = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
+
+    def timed_step():
+        if args.separate_gemms:
+            if args.serial_step:
+                step.run(stream)
+            else:
+                step.run_concurrent(stream, side)
+        else:
+            step.run_grouped(stream, None if args.serial_step else side)
+
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            step.run(stream)
+            timed_step()  # the form the timed region runs, so the parity gate checks its outputs
     stream.synchronize()
     if m.device_status() != 0:
         raise RuntimeError("device status word set during warm-up")
@@ -803,16 +842,14 @@ def main():
         return 3
 
     # --------------------------------------------------------------- timed region (HBM-resident inputs)
-    # One step (6 launches through the C ABI) is captured once as a CUDA graph
-    # and replayed K times, so the host never starves the GPU between launches.
+    # One step (4 launches through the C ABI: three casts and one grouped GEMM;
+    # 6 with --separate-gemms) is captured once as a CUDA graph and replayed K
+    # times, so the host never starves the GPU between launches.
     n_launch = len(step.launches(stream))
+    n_launch_step = n_launch if args.separate_gemms else 4
     graph = torch.cuda.CUDAGraph()
-    side = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
     with torch.cuda.graph(graph, stream=stream):
-        if args.serial_step:
-            step.run(stream)
-        else:
-            step.run_concurrent(stream, side)
+        timed_step()
     with torch.cuda.stream(stream):
         for _ in range(3):
             graph.replay()
@@ -860,6 +897,16 @@ def main():
         stream.synchronize()
         if host_enqueue < sleep_s:
             break
+    # the grouped GEMM launch alone, eager, back to back behind a GPU sleep
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_prof)]
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int((0.005 + 2.0 * n_prof * host_per_step) * 2.2e9))
+        for i in range(n_prof):
+            gev[i][0].record(stream)
+            step.gemms_grouped(stream)
+            gev[i][1].record(stream)
+    stream.synchronize()
+    grouped_t = [a.elapsed_time(b) / 1e3 for a, b in gev]
     kinds = [k for k, _ in step.launches(stream)]
     per = [[evs[i][j][0].elapsed_time(evs[i][j][1]) / 1e3 for j in range(n_launch)] for i in range(n_prof)]
     gemm_t = [sum(p[j] for j in range(n_launch) if kinds[j] == "gemm") for p in per]
@@ -868,15 +915,25 @@ def main():
 
     peaks = load_peaks()
     fp4_peak = peaks["bf16"] * NOMINAL_FP4_OVER_BF16
-    gemm_mean_launch = statistics.mean(gemm_t) / 3.0
-    achieved = (STEP_FLOPS / 3.0) / gemm_mean_launch / 1e12
-    traffic = profiled_traffic()
+    if args.separate_gemms:
+        gemm_launch_s = statistics.mean(gemm_t) / 3.0      # mean of the three gemm_fp4 launches
+        achieved = (STEP_FLOPS / 3.0) / gemm_launch_s / 1e12
+        traffic = profiled_traffic("separate")
+        roof_kernel = "gemm_mxf4_pair_kernel (mean of the fwd/dgrad/wgrad gemm_fp4 launches)"
+    else:
+        gemm_launch_s = statistics.mean(grouped_t)          # the one grouped launch of the step
+        achieved = STEP_FLOPS / gemm_launch_s / 1e12
+        traffic = profiled_traffic("grouped")
+        roof_kernel = "gemm_mxf4_pair_kernel (the grouped fwd + dgrad + wgrad launch)"
     cast_bytes = sum(CAST_ELEMS) * CAST_BYTES_PER_ELEM
     cast_gbs = cast_bytes / statistics.mean(cast_t) / 1e9
     gemm_names = ["fwd", "dgrad", "wgrad"]
     breakdown = {
         "gemm_tflops": {gemm_names[i]: GEMM_FLOPS[i] / launch_mean[3 + i] / 1e12 for i in range(3)},
         "gemm_us": {gemm_names[i]: launch_mean[3 + i] * 1e6 for i in range(3)},
+        "gemm_separate_us_sum": sum(launch_mean[3:6]) * 1e6,
+        "gemm_grouped_us": statistics.mean(grouped_t) * 1e6,
+        "gemm_grouped_tflops": STEP_FLOPS / statistics.mean(grouped_t) / 1e12,
         "cast_gbs": {n: CAST_ELEMS[i] * CAST_BYTES_PER_ELEM / launch_mean[i] / 1e9 for i, n in enumerate(["X", "W", "dY"])},
         "cast_us": {n: launch_mean[i] * 1e6 for i, n in enumerate(["X", "W", "dY"])},
         "cast_gbs_all": cast_gbs,
@@ -946,7 +1003,7 @@ def main():
             "config": bench_config(world),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s",
                          "frac": achieved / fp4_peak, "traffic": traffic,
-                         "kernel": "gemm_mxf4_kernel (mean of the fwd/dgrad/wgrad launches)",
+                         "kernel": roof_kernel,
                          "peak_source": f"{peaks['source']} bf16 burst {peaks['bf16']:.1f} TFLOP/s x nominal "
                                         f"dense fp4/bf16 ratio {NOMINAL_FP4_OVER_BF16:.0f}"},
             "parity": parity,
@@ -954,11 +1011,14 @@ def main():
             "cpu_baseline": cpu,
             **({"extra": extra} if extra else {}),
             "e2e": e2e,
-            "gpu_launches": n_launch * args.steps,
-            "timing": {"timed_region": ("CUDA-graph replay of the captured step, K times, CUDA events on the launch stream"
-                                 + ("" if args.serial_step else "; the step's independent launches on three "
-                                    "streams (three casts side by side, each GEMM after its two casts)")),
-                       "per_kernel": f"{n_prof} eager steps enqueued behind a GPU sleep, an event pair per launch"},
+            "gpu_launches": n_launch_step * args.steps,
+            "timing": {"timed_region": ("CUDA-graph replay of the captured step, K times, CUDA events on the launch stream; "
+                                        + ("six launches (three gemm_fp4)" if args.separate_gemms else
+                                           "four launches (three casts, one gemm_fp4_grouped of fwd, dgrad and wgrad)")
+                                        + ("" if args.serial_step else
+                                           ", the casts side by side on three streams")),
+                       "per_kernel": f"{n_prof} eager steps of six launches, and {n_prof} eager grouped GEMM launches, "
+                                     "each enqueued behind a GPU sleep, an event pair per launch"},
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)

@@ -136,6 +136,36 @@ mxfp4_status gemm_fp4(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, c
                       uint16_t* c, int64_t M, int64_t N, int64_t K, int64_t ldc, void* stream);
 
 /*
+ * gemm_fp4_grouped -- up to MXFP4_GROUP_MAX independent gemm_fp4 calls in one
+ * launch.  The "FP4 GEMM (training)" row runs the forward GEMM, dA and dB
+ * through gemm_fp4. In a training step their operands are ready together,
+ * and one persistent launch over all their tiles (numbered GEMM after GEMM)
+ * leaves a single partial last wave of tiles where separate launches leave
+ * one each.  The pages describe no grouped call: this is a scheduling form of
+ * gemm_fp4 with the same results, each C bit-identical to the gemm_fp4 call
+ * with the same arguments.
+ *   gemms : host array of `count` descriptors, read during the call only; each
+ *           field means what the gemm_fp4 argument of the same name means
+ *   count : 1 .. MXFP4_GROUP_MAX
+ * Each descriptor is checked as gemm_fp4 checks its arguments, in that
+ * order. The first failing descriptor's status is returned and nothing is
+ * launched. Descriptors with M == 0 or N == 0 are skipped; K == 0 writes
+ * zeros. Every GEMM's memory must be on one device (MXFP4_ERR_INVALID_ARG
+ * otherwise). The GEMMs run concurrently: no C may overlap another
+ * descriptor's C or operands.
+ */
+#define MXFP4_GROUP_MAX 4
+typedef struct mxfp4_gemm_desc {
+  const uint8_t* a;
+  const uint8_t* a_sf;
+  const uint8_t* b;
+  const uint8_t* b_sf;
+  uint16_t* c;
+  int64_t M, N, K, ldc;
+} mxfp4_gemm_desc;
+mxfp4_status gemm_fp4_grouped(const mxfp4_gemm_desc* gemms, int count, void* stream);
+
+/*
  * gemm_fp4_cast_out -- gemm_fp4 whose epilogue also casts its own output to
  * MXFP4, so the next GEMM's operand comes without a separate cast of C (the
  * gradient one GEMM produces is the next one's grad_out: jax-aiter README,

@@ -28,6 +28,14 @@ MXFP4_HADAMARD_ROW = 1
 MXFP4_HADAMARD_COL = 2
 MXFP4_SCALE_LINEAR = 4
 MXFP4_OP_FWD, MXFP4_OP_DGRAD, MXFP4_OP_WGRAD, MXFP4_OP_WGRAD_FP8 = 0, 1, 2, 3
+MXFP4_GROUP_MAX = 4
+
+
+class GemmDesc(ctypes.Structure):
+    """mxfp4_gemm_desc: one GEMM of a gemm_fp4_grouped call."""
+    _fields_ = [("a", ctypes.c_void_p), ("a_sf", ctypes.c_void_p), ("b", ctypes.c_void_p),
+                ("b_sf", ctypes.c_void_p), ("c", ctypes.c_void_p), ("M", ctypes.c_int64),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("ldc", ctypes.c_int64)]
 
 # Every extern "C" symbol declared in include/mxfp4.h.
 ABI_SYMBOLS = (
@@ -36,7 +44,7 @@ ABI_SYMBOLS = (
     "gemm_fp4_bf16_fwd", "gemm_fp4_bf16_dgrad", "gemm_fp4_bf16_wgrad", "mxfp4_device_status",
     "gemm_fp4_bf16_fwd_noalloc", "mxfp4_last_cuda_error", "mxfp4_cuda_error_string",
     "mxfp8_cast_cols", "gemm_mxfp8", "gemm_fp8_bf16_wgrad", "gemm_fp4_cast_out",
-    "mxfp4_selftest_wait_timeout",
+    "mxfp4_selftest_wait_timeout", "gemm_fp4_grouped",
 )
 
 _lib = None
@@ -86,6 +94,7 @@ def lib() -> ctypes.CDLL:
                 "mxfp4_cuda_error_string": (ctypes.c_char_p, [I]),
                 "gemm_fp4_cast_out": (I, [P, P, P, P, P, I64, I64, I64, I64, P, P, P, P, U32, P]),
                 "mxfp4_selftest_wait_timeout": (I, [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_uint64, P]),
+                "gemm_fp4_grouped": (I, [ctypes.POINTER(GemmDesc), I, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -186,6 +195,25 @@ def gemm_fp4(a, a_sf, b, b_sf, M: int, N: int, K: int, c=None, stream=None):
     _check(lib().gemm_fp4(_ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), _ptr(c), M, N, K, c.stride(0),
                           _stream(stream)), "gemm_fp4")
     return c
+
+
+def gemm_fp4_grouped(gemms, stream=None):
+    """Independent GEMMs in one launch: `gemms` is a sequence of up to
+    MXFP4_GROUP_MAX tuples (a, a_sf, b, b_sf, M, N, K) or (a, a_sf, b, b_sf,
+    M, N, K, c), each as gemm_fp4's arguments.  Returns the list of C."""
+    gemms = list(gemms)
+    descs = (GemmDesc * max(1, len(gemms)))()
+    outs = []
+    for i, g in enumerate(gemms):
+        a, a_sf, b, b_sf, M, N, K = g[:7]
+        c = g[7] if len(g) > 7 else None
+        _need_cuda(a, a_sf, b, b_sf)
+        if c is None:
+            c = torch.empty(M, N, dtype=torch.bfloat16, device=a.device)
+        descs[i] = GemmDesc(_ptr(a), _ptr(a_sf), _ptr(b), _ptr(b_sf), _ptr(c), M, N, K, c.stride(0))
+        outs.append(c)
+    _check(lib().gemm_fp4_grouped(descs, len(gemms), _stream(stream)), "gemm_fp4_grouped")
+    return outs
 
 
 def gemm_fp4_cast_out(a, a_sf, b, b_sf, M: int, N: int, K: int, row=True, col=True,

@@ -158,6 +158,29 @@ size_t carve_fp8_bytes(int64_t rows, int64_t cols) {
          align256(tile_scale_bytes(rows, cols));
 }
 
+// The argument checks of gemm_fp4, in order; on MXFP4_OK the device of c is
+// bound (nothing to check or bind when *empty: M == 0 or N == 0).
+mxfp4_status check_gemm(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, const uint8_t* b_sf,
+                        const uint16_t* c, int64_t M, int64_t N, int64_t K, int64_t ldc, bool* empty) {
+  *empty = false;
+  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+    return MXFP4_ERR_INVALID_ARG;
+  if (K % 32 != 0 || ldc < N) return MXFP4_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) {
+    *empty = true;
+    return MXFP4_OK;
+  }
+  MXFP4_TRY(check_out(c));
+  if (ldc % 8 != 0) return MXFP4_ERR_MISALIGNED;
+  if (K > 0) {
+    MXFP4_TRY(check_out(a));
+    MXFP4_TRY(check_out(a_sf));
+    MXFP4_TRY(check_out(b));
+    MXFP4_TRY(check_out(b_sf));
+  }
+  return check_device(c);
+}
+
 mxfp4_status gemm_checked(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b,
                           const uint8_t* b_sf, uint16_t* c, int64_t M, int64_t N, int64_t K,
                           int64_t ldc, cudaStream_t s, bool fp8 = false) {
@@ -235,20 +258,32 @@ mxfp4_status mxfp4_cast_dual(const uint16_t* x, int64_t rows, int64_t cols, int6
 
 mxfp4_status gemm_fp4(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, const uint8_t* b_sf,
                       uint16_t* c, int64_t M, int64_t N, int64_t K, int64_t ldc, void* stream) {
-  if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
-    return MXFP4_ERR_INVALID_ARG;
-  if (K % 32 != 0 || ldc < N) return MXFP4_ERR_INVALID_ARG;
-  if (M == 0 || N == 0) return MXFP4_OK;
-  MXFP4_TRY(check_out(c));
-  if (ldc % 8 != 0) return MXFP4_ERR_MISALIGNED;
-  if (K > 0) {
-    MXFP4_TRY(check_out(a));
-    MXFP4_TRY(check_out(a_sf));
-    MXFP4_TRY(check_out(b));
-    MXFP4_TRY(check_out(b_sf));
-  }
-  MXFP4_TRY(check_device(c));
+  bool empty = false;
+  MXFP4_TRY(check_gemm(a, a_sf, b, b_sf, c, M, N, K, ldc, &empty));
+  if (empty) return MXFP4_OK;
   return gemm_checked(a, a_sf, b, b_sf, c, M, N, K, ldc, static_cast<cudaStream_t>(stream));
+}
+
+mxfp4_status gemm_fp4_grouped(const mxfp4_gemm_desc* gemms, int count, void* stream) {
+  if (gemms == nullptr || count < 1 || count > MXFP4_GROUP_MAX) return MXFP4_ERR_INVALID_ARG;
+  GemmArgs list[MXFP4_GROUP_MAX];
+  int n = 0, dev = -1;
+  for (int i = 0; i < count; ++i) {
+    const mxfp4_gemm_desc& d = gemms[i];
+    bool empty = false;
+    MXFP4_TRY(check_gemm(d.a, d.a_sf, d.b, d.b_sf, d.c, d.M, d.N, d.K, d.ldc, &empty));
+    if (empty) continue;
+    int cur = 0;
+    cudaError_t e = cudaGetDevice(&cur);  // the device check_gemm bound
+    if (e != cudaSuccess) return from_cuda(e);
+    if (dev >= 0 && cur != dev) return MXFP4_ERR_INVALID_ARG;  // one launch, one device
+    dev = cur;
+    list[n++] = GemmArgs{d.a, d.a_sf, d.b, d.b_sf, d.c, d.M, d.N, d.K, d.ldc};
+  }
+  if (n == 0) return MXFP4_OK;
+  cudaError_t e = mxfp4::launch_gemm_grouped(list, n, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidValue) return MXFP4_ERR_INVALID_ARG;
+  return from_cuda(e);
 }
 
 mxfp4_status gemm_mxfp8(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, const uint8_t* b_sf,

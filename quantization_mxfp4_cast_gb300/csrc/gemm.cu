@@ -74,6 +74,7 @@ __device__ int g_device_status = 0;
 
 namespace {
 
+constexpr int kMaxGroup = 4;            // GEMMs per grouped launch
 constexpr int kBM = 256;                // rows of C per CTA pair
 constexpr int kRowsPerCta = 128;        // rows of A (and of B) held by each CTA
 constexpr int kBN = 256;                // columns of C per tile
@@ -149,10 +150,28 @@ __device__ __forceinline__ void tile_coords(int t, int num_mt, int num_nt, int g
   nt = r / gm;
 }
 
-struct PairGemmParams {
-  GemmArgs args;
+// Tile counts of one GEMM of the launch.  A launch runs up to kMaxGroup
+// independent GEMMs (gemm_fp4_grouped): their tiles are numbered one after
+// the other, GEMM g owning [tile_end[g-1], tile_end[g]).
+struct GroupTiles {
   int num_mt, num_nt, num_kt, ktiles128;
-  int group_m;  // raster group, in pair row tiles
+  int group_m;   // raster group, in pair row tiles
+  int last_nks;  // 64-deep k-steps of the last stage (K % 64 == 32 rounds up: zero codes)
+  int tile_end;  // one past the GEMM's last tile in the launch's numbering
+  int has_c;     // 0: no bf16 C (the cast-only form of the output-cast instance)
+};
+
+// Tensor maps of a launch: operands, scales and C of each GEMM, and the
+// output-cast code maps (kCastOut instance, one GEMM).
+struct GemmMaps {
+  CUtensorMap a[kMaxGroup], b[kMaxGroup], sfa[kMaxGroup], sfb[kMaxGroup], c[kMaxGroup];
+  CUtensorMap qr, qc;
+};
+
+struct PairGemmParams {
+  GroupTiles g[kMaxGroup];
+  int groups;     // GEMMs in the launch, 1..kMaxGroup
+  int num_tiles;  // tiles of all of them
   // output cast (kCastOut instance): tile-layout scales of C along N and of
   // C^T along M (each null when that output is not wanted), Hadamard flags,
   // and the scale tile counts ceil(M / 128), ceil(N / 128)
@@ -168,16 +187,20 @@ struct PairGemmParams {
   int withhold_first_scale_signal;
 };
 
+// The GEMM that owns launch tile t, and t's index within that GEMM.
+__device__ __forceinline__ int tile_group(const PairGemmParams& p, int t, int& lt) {
+  int g = 0, begin = 0;
+  while (g + 1 < p.groups && t >= p.g[g].tile_end) {
+    begin = p.g[g].tile_end;
+    ++g;
+  }
+  lt = t - begin;
+  return g;
+}
+
 template <bool kFp8, bool kCastOut>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_mxf4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                          const __grid_constant__ CUtensorMap tmB,
-                          const __grid_constant__ CUtensorMap tmSfa,
-                          const __grid_constant__ CUtensorMap tmSfb,
-                          const __grid_constant__ CUtensorMap tmC,
-                          const __grid_constant__ CUtensorMap tmQr,  // row codes of C (kCastOut)
-                          const __grid_constant__ CUtensorMap tmQc,  // column codes of C (kCastOut)
-                          const PairGemmParams p) {
+    gemm_mxf4_pair_kernel(const __grid_constant__ GemmMaps maps, const PairGemmParams p) {
   using F = Fmt<kFp8, kCastOut>;
   constexpr int kStages = F::kStages;
   constexpr int kSfaStage = F::kSfaStage, kSfbStage = F::kSfbStage;
@@ -211,7 +234,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_cta_rank();  // 0 = the CTA that issues the MMAs
   const bool leader = rank == 0;
-  const GemmArgs& args = p.args;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -227,14 +249,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmSfa);
-    tma_prefetch_desc(&tmSfb);
-    tma_prefetch_desc(&tmC);
+    for (int g = 0; g < p.groups; ++g) {
+      tma_prefetch_desc(&maps.a[g]);
+      tma_prefetch_desc(&maps.b[g]);
+      tma_prefetch_desc(&maps.sfa[g]);
+      tma_prefetch_desc(&maps.sfb[g]);
+      if (p.g[g].has_c) tma_prefetch_desc(&maps.c[g]);
+    }
     if constexpr (kCastOut) {
-      if (p.sf_row != nullptr) tma_prefetch_desc(&tmQr);
-      if (p.sf_col != nullptr) tma_prefetch_desc(&tmQc);
+      if (p.sf_row != nullptr) tma_prefetch_desc(&maps.qr);
+      if (p.sf_col != nullptr) tma_prefetch_desc(&maps.qc);
     }
   }
   if (warp == 1) {
@@ -245,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // barriers of both CTAs initialized before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int num_tiles = p.num_mt * p.num_nt;
+  const int num_tiles = p.num_tiles;
   const int pair = static_cast<int>(blockIdx.x >> 1);
   const int num_pairs = static_cast<int>(gridDim.x >> 1);
 
@@ -256,25 +280,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int issued = 0;  // stage loads issued so far
       for (int t = pair; ok && t < num_tiles; t += num_pairs) {
-        int mt, nt;
-        tile_coords(t, p.num_mt, p.num_nt, p.group_m, mt, nt);
+        int lt, mt, nt;
+        const int g = tile_group(p, t, lt);
+        const GroupTiles& G = p.g[g];
+        tile_coords(lt, G.num_mt, G.num_nt, G.group_m, mt, nt);
         const int a_row = mt * kBM + static_cast<int>(rank) * kRowsPerCta;
         const int b_row = nt * kBN + static_cast<int>(rank) * kRowsPerCta;
         const int a_rt = a_row / 128;  // this CTA's scale row tile of A
-        for (int kt = 0; kt < p.num_kt; ++kt) {
+        for (int kt = 0; kt < G.num_kt; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, &g_device_status, p.wait_limit_ns)) {
             ok = false;
             break;
           }
           const int kg0 = kt * F::kKTiles;
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
-          tma_load_2d(sA + stage * kAStage, &tmA, &full[stage], kt * kBKBytes, a_row);
-          tma_load_2d(sB + stage * kBStage, &tmB, &full[stage], kt * kBKBytes, b_row);
-          tma_load_2d(sSfa + stage * kSfaStage, &tmSfa, &full[stage], 0,
-                      (a_rt * p.ktiles128 + kg0) * 4);
+          tma_load_2d(sA + stage * kAStage, &maps.a[g], &full[stage], kt * kBKBytes, a_row);
+          tma_load_2d(sB + stage * kBStage, &maps.b[g], &full[stage], kt * kBKBytes, b_row);
+          tma_load_2d(sSfa + stage * kSfaStage, &maps.sfa[g], &full[stage], 0,
+                      (a_rt * G.ktiles128 + kg0) * 4);
           // both 128-row scale tiles of B in one box (measured: 4-7% faster
           // than two 2-D loads)
-          tma_load_3d(sSfb + stage * kSfbStage, &tmSfb, &full[stage], 0, kg0 * 4, nt * 2);
+          tma_load_3d(sSfb + stage * kSfbStage, &maps.sfb[g], &full[stage], 0, kg0 * 4, nt * 2);
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -303,14 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint64_t adesc0 = make_smem_desc(smem_u32(sA), 16, 1024, 2);
       const uint64_t bdesc0 = make_smem_desc(smem_u32(sB), 16, 1024, 2);
-      // 64-deep k-steps of the last stage (K % 64 == 32 rounds up: zero codes).
-      const int last_nks = static_cast<int>(
-          (args.K - static_cast<int64_t>(p.num_kt - 1) * F::kBK + F::kMmaK - 1) / F::kMmaK);
       for (int t = pair; ok && t < num_tiles; t += num_pairs) {
+        int lt;
+        const GroupTiles& G = p.g[tile_group(p, t, lt)];
         ok = mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, &g_device_status, p.wait_limit_ns);
         if (!__all_sync(0xFFFFFFFFu, ok)) break;
         tc_fence_after();
-        for (int kt = 0; kt < p.num_kt; ++kt) {
+        for (int kt = 0; kt < G.num_kt; ++kt) {
           ok = mbar_wait(&sf_ready[stage], phase, abort_flag, &g_device_status, p.wait_limit_ns);
           if (!__all_sync(0xFFFFFFFFu, ok)) {
             ok = false;
@@ -322,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t a_d = adesc0 + ((stage * kAStage) >> 4);
           const uint64_t b_d = bdesc0 + ((stage * kBStage) >> 4);
           const uint32_t sf_col = tmem_base + kSfCol0 + stage * kSfStageCols;
-          const int nks = kt + 1 < p.num_kt ? 4 : last_nks;
+          const int nks = kt + 1 < G.num_kt ? 4 : G.last_nks;
           if (elect_one_sync()) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
@@ -373,7 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stage = 0, phase = 0;
     bool ok = true;
     for (int t = pair; ok && t < num_tiles; t += num_pairs) {
-      for (int kt = 0; kt < p.num_kt; ++kt) {
+      int lt;
+      const int num_kt = p.g[tile_group(p, t, lt)].num_kt;
+      for (int kt = 0; kt < num_kt; ++kt) {
         if (!mbar_wait(&full[stage], phase, abort_flag, &g_device_status, p.wait_limit_ns)) {
           ok = false;
           break;
@@ -423,8 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool had_col = (p.cast_flags & kFlagHadamardCol) != 0;
     uint32_t acc_phase = 0;
     for (int t = pair; t < num_tiles; t += num_pairs) {
-      int mt, nt;
-      tile_coords(t, p.num_mt, p.num_nt, p.group_m, mt, nt);
+      int lt, mt, nt;
+      const int g = tile_group(p, t, lt);
+      const GroupTiles& G = p.g[g];
+      tile_coords(lt, G.num_mt, G.num_nt, G.group_m, mt, nt);
       if (!mbar_wait(acc_full, acc_phase, abort_flag, &g_device_status, p.wait_limit_ns)) break;
       tc_fence_after();
       // Read all 128 columns (4 x 32) as bf16 pairs, then release the accumulator.
@@ -464,8 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) {
-          if (!kCastOut || p.args.c != nullptr)  // the cast-only form writes no bf16 C
-            tma_store_2d(&tmC, sOut + ew * kOutStageBytes, col0 + c * 32, row0);
+          if (G.has_c)  // the cast-only form writes no bf16 C
+            tma_store_2d(&maps.c[g], sOut + ew * kOutStageBytes, col0 + c * 32, row0);
           bulk_commit_group();
         }
         if constexpr (kCastOut) {
@@ -522,8 +551,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0 && (do_row || do_col)) {
-          if (do_row) tma_store_2d(&tmQr, sOut + (kEpiWarps + ew) * kOutStageBytes, col0 / 2, row0);
-          if (do_col) tma_store_2d(&tmQc, sOut + (2 * kEpiWarps + ew) * kOutStageBytes, row0 / 2, col0);
+          if (do_row) tma_store_2d(&maps.qr, sOut + (kEpiWarps + ew) * kOutStageBytes, col0 / 2, row0);
+          if (do_col) tma_store_2d(&maps.qc, sOut + (2 * kEpiWarps + ew) * kOutStageBytes, row0 / 2, col0);
           bulk_commit_group();
         }
         // scales of this lane's row: blocks 0-3 of the 128-column tile, one word
@@ -688,71 +717,97 @@ cudaError_t launch_fill_zero_bf16(uint16_t* c, int64_t M, int64_t N, int64_t ldc
 
 namespace {
 
+// One launch over the tiles of `count` independent GEMMs (1..kMaxGroup; the
+// output-cast instance takes one).  GEMMs with M or N == 0 are skipped; those
+// with K == 0 get C = 0 (and zero casts) from separate fills, enqueued first.
 template <bool kFp8, bool kCastOut = false>
-cudaError_t launch_gemm_fmt(const GemmArgs& args, cudaStream_t stream, const CastOutArgs* out = nullptr,
+cudaError_t launch_gemm_fmt(const GemmArgs* list, int count, cudaStream_t stream,
+                            const CastOutArgs* out = nullptr,
                             unsigned long long wait_limit_ns = kWaitLimitNs, bool withhold = false) {
   using F = Fmt<kFp8, kCastOut>;
-  if (args.M == 0 || args.N == 0) return cudaSuccess;
-  if (args.K == 0) {  // C = 0, and its casts are those of a zero matrix: all bytes 0x00
-    cudaError_t e = args.c != nullptr ? launch_fill_zero_bf16(args.c, args.M, args.N, args.ldc, stream)
-                                      : cudaSuccess;
-    if (e != cudaSuccess || !kCastOut) return e;
-    const size_t code_bytes = static_cast<size_t>(args.M) * static_cast<size_t>(args.N / 2);
-    const size_t sf_bytes = static_cast<size_t>((args.M + 127) / 128) * ((args.N + 127) / 128) * 512;
-    if (out->q_row != nullptr && e == cudaSuccess) e = cudaMemsetAsync(out->q_row, 0, code_bytes, stream);
-    if (out->sf_row != nullptr && e == cudaSuccess) e = cudaMemsetAsync(out->sf_row, 0, sf_bytes, stream);
-    if (out->q_col != nullptr && e == cudaSuccess) e = cudaMemsetAsync(out->q_col, 0, code_bytes, stream);
-    if (out->sf_col != nullptr && e == cudaSuccess) e = cudaMemsetAsync(out->sf_col, 0, sf_bytes, stream);
-    return e;
+  if (count < 1 || count > kMaxGroup || (kCastOut && count != 1)) return cudaErrorInvalidValue;
+  GemmMaps maps = {};
+  PairGemmParams p = {};
+  int64_t tiles = 0;
+  int groups = 0;
+  for (int i = 0; i < count; ++i) {
+    const GemmArgs& args = list[i];
+    if (args.M == 0 || args.N == 0) continue;
+    if (args.K == 0) {  // C = 0, and its casts are those of a zero matrix: all bytes 0x00
+      cudaError_t e = args.c != nullptr ? launch_fill_zero_bf16(args.c, args.M, args.N, args.ldc, stream)
+                                        : cudaSuccess;
+      if (e != cudaSuccess) return e;
+      if (kCastOut) {
+        const size_t code_bytes = static_cast<size_t>(args.M) * static_cast<size_t>(args.N / 2);
+        const size_t sf_bytes = static_cast<size_t>((args.M + 127) / 128) * ((args.N + 127) / 128) * 512;
+        if (out->q_row != nullptr && e == cudaSuccess) e = cudaMemsetAsync(out->q_row, 0, code_bytes, stream);
+        if (out->sf_row != nullptr && e == cudaSuccess) e = cudaMemsetAsync(out->sf_row, 0, sf_bytes, stream);
+        if (out->q_col != nullptr && e == cudaSuccess) e = cudaMemsetAsync(out->q_col, 0, code_bytes, stream);
+        if (out->sf_col != nullptr && e == cudaSuccess) e = cudaMemsetAsync(out->sf_col, 0, sf_bytes, stream);
+        if (e != cudaSuccess) return e;
+      }
+      continue;
+    }
+    const int64_t ktiles128 = (args.K + 127) / 128;
+    const int64_t a_sf_rows = (args.M + 127) / 128 * ktiles128 * 4;  // 128-byte rows of the scale buffer
+    const int64_t row_bytes = kFp8 ? args.K : args.K / 2;             // code bytes per row
+    const int g = groups;
+    if (!make_byte_map(&maps.a[g], args.a, args.M, row_bytes, kBKBytes, kRowsPerCta,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_byte_map(&maps.b[g], args.b, args.N, row_bytes, kBKBytes, kRowsPerCta,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_byte_map(&maps.sfa[g], args.a_sf, a_sf_rows, 128, 128, 4 * F::kKTiles,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_scale_pair_map(&maps.sfb[g], args.b_sf, (args.N + 127) / 128, ktiles128, 4 * F::kKTiles))
+      return cudaErrorInvalidValue;
+    if (args.c != nullptr && !make_bf16_out_map(&maps.c[g], args.c, args.M, args.N, args.ldc))
+      return cudaErrorInvalidValue;
+    GroupTiles& G = p.g[g];
+    G.num_mt = static_cast<int>((args.M + kBM - 1) / kBM);
+    G.num_nt = static_cast<int>((args.N + kBN - 1) / kBN);
+    G.num_kt = static_cast<int>((args.K + F::kBK - 1) / F::kBK);
+    G.ktiles128 = static_cast<int>(ktiles128);
+    G.last_nks = static_cast<int>((args.K - static_cast<int64_t>(G.num_kt - 1) * F::kBK + F::kMmaK - 1) /
+                                  F::kMmaK);
+    // Raster group: powers of two up to 64 row tiles while the group's A panel,
+    // counted in FP4 bytes (K / 2 per row), stays within the budget.  An MXFP8
+    // panel of the same K is twice the bytes and still fits the L2; sizing it
+    // by its own bytes halved the group and streamed B twice (measured on the
+    // wgrad of the 8B down projection: 1.8x the operand bytes read from DRAM).
+    G.group_m = 1;
+    while (G.group_m < 64 && 2 * G.group_m * kBM * (args.K / 2) <= kRasterPanelBytes) G.group_m *= 2;
+    G.has_c = args.c != nullptr ? 1 : 0;
+    tiles += static_cast<int64_t>(G.num_mt) * G.num_nt;
+    if (tiles > (int64_t(1) << 30)) return cudaErrorInvalidValue;
+    G.tile_end = static_cast<int>(tiles);
+    ++groups;
   }
-  const int64_t ktiles128 = (args.K + 127) / 128;
-  const int64_t a_sf_rows = (args.M + 127) / 128 * ktiles128 * 4;  // 128-byte rows of the scale buffer
-  const int64_t row_bytes = kFp8 ? args.K : args.K / 2;             // code bytes per row
-
-  CUtensorMap tmA, tmB, tmSfa, tmSfb;
-  if (!make_byte_map(&tmA, args.a, args.M, row_bytes, kBKBytes, kRowsPerCta, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_byte_map(&tmB, args.b, args.N, row_bytes, kBKBytes, kRowsPerCta, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_byte_map(&tmSfa, args.a_sf, a_sf_rows, 128, 128, 4 * F::kKTiles, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_scale_pair_map(&tmSfb, args.b_sf, (args.N + 127) / 128, ktiles128, 4 * F::kKTiles))
-    return cudaErrorInvalidValue;
-  CUtensorMap tmC = {};
-  if (args.c != nullptr && !make_bf16_out_map(&tmC, args.c, args.M, args.N, args.ldc))
-    return cudaErrorInvalidValue;
-  // output cast: row codes [M, N/2] in 32-row x 64-byte boxes (64-byte
-  // swizzle), column codes [N, M/2] in 128-row x 16-byte boxes
-  CUtensorMap tmQr = {}, tmQc = {};
-  if (kCastOut && out->q_row != nullptr &&
-      !make_byte_map(&tmQr, out->q_row, args.M, args.N / 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_64B))
-    return cudaErrorInvalidValue;
-  if (kCastOut && out->q_col != nullptr &&
-      !make_byte_map(&tmQc, out->q_col, args.N, args.M / 2, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
-    return cudaErrorInvalidValue;
+  if (groups == 0) return cudaSuccess;
+  p.groups = groups;
+  p.num_tiles = static_cast<int>(tiles);
+  if constexpr (kCastOut) {
+    // output cast: row codes [M, N/2] in 32-row x 64-byte boxes (64-byte
+    // swizzle), column codes [N, M/2] in 128-row x 16-byte boxes
+    const GemmArgs& args = list[0];
+    if (out->q_row != nullptr &&
+        !make_byte_map(&maps.qr, out->q_row, args.M, args.N / 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+    if (out->q_col != nullptr &&
+        !make_byte_map(&maps.qc, out->q_col, args.N, args.M / 2, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    p.sf_row = out->sf_row;
+    p.sf_col = out->sf_col;
+    p.cast_flags = out->flags;
+    p.m_tiles128 = static_cast<int>((args.M + 127) / 128);
+    p.n_tiles128 = static_cast<int>((args.N + 127) / 128);
+  }
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = prepare_kernel<kFp8, kCastOut>(dev);
   if (e != cudaSuccess) return e;
-  PairGemmParams p;
-  p.args = args;
-  p.num_mt = static_cast<int>((args.M + kBM - 1) / kBM);
-  p.num_nt = static_cast<int>((args.N + kBN - 1) / kBN);
-  p.num_kt = static_cast<int>((args.K + F::kBK - 1) / F::kBK);
-  p.ktiles128 = static_cast<int>(ktiles128);
-  // Raster group: powers of two up to 64 row tiles while the group's A panel,
-  // counted in FP4 bytes (K / 2 per row), stays within the budget.  An MXFP8
-  // panel of the same K is twice the bytes and still fits the L2; sizing it
-  // by its own bytes halved the group and streamed B twice (measured on the
-  // wgrad of the 8B down projection: 1.8x the operand bytes read from DRAM).
-  p.group_m = 1;
-  while (p.group_m < 64 && 2 * p.group_m * kBM * (args.K / 2) <= kRasterPanelBytes) p.group_m *= 2;
-  p.sf_row = kCastOut ? out->sf_row : nullptr;
-  p.sf_col = kCastOut ? out->sf_col : nullptr;
-  p.cast_flags = kCastOut ? out->flags : 0u;
-  p.m_tiles128 = static_cast<int>((args.M + 127) / 128);
-  p.n_tiles128 = static_cast<int>((args.N + 127) / 128);
   p.wait_limit_ns = wait_limit_ns;
   p.withhold_first_scale_signal = withhold ? 1 : 0;
-  const int64_t tiles = static_cast<int64_t>(p.num_mt) * p.num_nt;
   const int pairs = static_cast<int>(std::min<int64_t>(tiles, max_pairs<kFp8, kCastOut>(dev)));
 
   cudaLaunchConfig_t cfg = {};
@@ -768,25 +823,30 @@ cudaError_t launch_gemm_fmt(const GemmArgs& args, cudaStream_t stream, const Cas
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // the launch's own result (the thread's last error may be stale and unrelated)
-  return cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel<kFp8, kCastOut>, tmA, tmB, tmSfa, tmSfb, tmC, tmQr,
-                            tmQc, p);
+  return cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel<kFp8, kCastOut>, maps, p);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream) { return launch_gemm_fmt<false>(args, stream); }
+cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream) {
+  return launch_gemm_fmt<false>(&args, 1, stream);
+}
+
+cudaError_t launch_gemm_grouped(const GemmArgs* list, int count, cudaStream_t stream) {
+  return launch_gemm_fmt<false>(list, count, stream);
+}
 
 cudaError_t launch_gemm_mxfp8(const GemmArgs& args, cudaStream_t stream) {
-  return launch_gemm_fmt<true>(args, stream);
+  return launch_gemm_fmt<true>(&args, 1, stream);
 }
 
 cudaError_t launch_gemm_cast_out(const GemmArgs& args, const CastOutArgs& out, cudaStream_t stream) {
-  return launch_gemm_fmt<false, true>(args, stream, &out);
+  return launch_gemm_fmt<false, true>(&args, 1, stream, &out);
 }
 
 cudaError_t launch_gemm_selftest_timeout(const GemmArgs& args, unsigned long long wait_limit_ns,
                                          cudaStream_t stream) {
-  return launch_gemm_fmt<false>(args, stream, nullptr, wait_limit_ns, true);
+  return launch_gemm_fmt<false>(&args, 1, stream, nullptr, wait_limit_ns, true);
 }
 
 }  // namespace mxfp4

@@ -40,6 +40,9 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
+// Up to 4 independent GEMMs in one persistent launch (their tiles numbered
+// one after the other); cudaErrorInvalidValue for count outside 1..4.
+cudaError_t launch_gemm_grouped(const GemmArgs* list, int count, cudaStream_t stream);
 
 // The MXFP4 dual cast of the GEMM's own bf16 output, written by its epilogue.
 struct CastOutArgs {

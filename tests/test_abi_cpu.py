@@ -118,6 +118,20 @@ def test_argument_validation_before_any_launch(L):
     # no output at all (no C and no cast) is refused; no C with a cast output is fine to validate
     assert co(good, good, good, good, None, 64, 64, 64, 64, None, None, None, None, 0, None) == INV
     assert co(good, good, good, good, None, 64, 64, 64, 0, good, good, odd, good, 0, None) == MIS
+    # grouped GEMM: count 1..4, a non-null array, each descriptor checked as
+    # gemm_fp4 checks its arguments (the first failing one's status), empty
+    # descriptors skipped
+    from quantization_mxfp4_cast_gb300 import GemmDesc
+    D = lambda M, N, K, ldc, c=good, a=good: GemmDesc(a, good, good, good, c, M, N, K, ldc)
+    grp = lambda *ds: L.gemm_fp4_grouped((GemmDesc * len(ds))(*ds), len(ds), None)
+    assert L.gemm_fp4_grouped(None, 1, None) == INV
+    assert L.gemm_fp4_grouped((GemmDesc * 1)(D(0, 8, 64, 8)), 0, None) == INV
+    assert L.gemm_fp4_grouped((GemmDesc * 5)(*[D(0, 8, 64, 8)] * 5), 5, None) == INV
+    assert grp(D(8, 8, 48, 8)) == INV                       # K % 32
+    assert grp(D(0, 8, 64, 8), D(8, 12, 64, 12)) == MIS     # second descriptor: ldc % 8
+    assert grp(D(8, 8, 64, 8, a=odd)) == MIS                 # misaligned operand
+    assert grp(D(8, 8, 64, 8, c=None)) == INV                # missing output
+    assert grp(D(0, 8, 64, 8, c=None), D(8, 0, 64, 8, c=None)) == 0   # all empty: no-op
     st = ctypes.c_int(0)
     assert L.mxfp4_device_status(0, None) == INV
 

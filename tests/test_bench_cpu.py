@@ -24,9 +24,11 @@ def test_strip_comments_keeps_code_only():
 
 def test_profiled_traffic_follows_the_code_hash():
     b = load_bench()
-    t = b.profiled_traffic()
     text = open(os.path.join(ROOT, "profiles", "gemm_mxf4_llama8b_down_train_step.md")).read()
-    if b.gemm_source_hash() in text:
-        assert t is not None and t > 1e8   # DRAM bytes per GEMM launch, ~2e8 at the 8B shapes
-    else:
-        assert t is None
+    for mode, low in (("separate", 1e8), ("grouped", 3e8)):
+        t = b.profiled_traffic(mode)
+        if b.gemm_source_hash() in text and f"dram bytes per {'grouped launch' if mode == 'grouped' else 'launch'}" in text:
+            # DRAM bytes per gemm_fp4 launch, ~2e8 at the 8B shapes; per grouped launch ~6e8
+            assert t is not None and t > low
+        else:
+            assert t is None

@@ -241,3 +241,49 @@ def test_repeated_full_size_dgrad_is_bit_identical(m):
     for i, c in enumerate(outs[1:], 1):
         assert torch.equal(c, outs[0]), f"launch {i} differs from launch 0"
     assert torch.isfinite(outs[0].float()).all()
+
+
+def rand_operands(M, N, K, seed, dev="cuda"):
+    """Random codes and tile-layout scales (every code value, a spread of
+    power-of-two scales) for a gemm_fp4 call, generated on the device."""
+    import quantization_mxfp4_cast_gb300 as mod
+    g = torch.Generator(device=dev).manual_seed(seed)
+    u8 = lambda *shape, lo=0, hi=256: torch.randint(lo, hi, shape, dtype=torch.uint8, device=dev, generator=g)
+    return (u8(M, K // 2), u8(mod.scales_bytes(M, K), lo=0x76, hi=0x7A),
+            u8(N, K // 2), u8(mod.scales_bytes(N, K), lo=0x76, hi=0x7A))
+
+
+def test_grouped_gemm_is_bit_identical_to_separate_calls(m):
+    # One launch over the train step's three GEMMs of the 8B down projection
+    # (fwd 8192x4096x14336, dgrad 8192x14336x4096, wgrad 4096x14336x8192) and
+    # a ragged one with a K tail (K % 64 == 32): each C equal to its own
+    # gemm_fp4 call, tile for tile the same arithmetic.
+    shapes = [(8192, 4096, 14336), (8192, 14336, 4096), (4096, 14336, 8192), (200, 296, 1056)]
+    ops = [rand_operands(M, N, K, seed=11 + i) for i, (M, N, K) in enumerate(shapes)]
+    sep = [m.gemm_fp4(*o, M, N, K) for o, (M, N, K) in zip(ops, shapes)]
+    grouped = m.gemm_fp4_grouped([(*o, M, N, K) for o, (M, N, K) in zip(ops, shapes)])
+    torch.cuda.synchronize()
+    for (M, N, K), a, b in zip(shapes, sep, grouped):
+        assert torch.equal(a, b), f"{M}x{N}x{K}"
+    # and the ragged one against the oracle
+    M, N, K = shapes[3]
+    ca, sa, cb, sb = (t.cpu().numpy() for t in ops[3])
+    ref = oracle.gemm_mxfp4(ca, oracle.sf_tile_to_linear(sa, M, K // 32), cb, oracle.sf_tile_to_linear(sb, N, K // 32),
+                            nthreads=8)
+    assert_close(grouped[3].float().cpu().numpy().astype(np.float64), ref, "grouped ragged")
+
+
+def test_grouped_gemm_edge_cases(m):
+    # a single descriptor; a group with an empty GEMM (skipped) and a K == 0
+    # GEMM (zeros) beside a real one; results equal to gemm_fp4's
+    o1 = rand_operands(384, 640, 1056, seed=5)
+    c1 = m.gemm_fp4_grouped([(*o1, 384, 640, 1056)])[0]
+    assert torch.equal(c1, m.gemm_fp4(*o1, 384, 640, 1056))
+    o2 = rand_operands(256, 512, 512, seed=6)
+    empty = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    zero_k = torch.full((128, 64), 1.0, dtype=torch.bfloat16, device="cuda")
+    z = torch.zeros(1, dtype=torch.uint8, device="cuda")
+    outs = m.gemm_fp4_grouped([(z, z, z, z, 0, 64, 64, empty), (*o2, 256, 512, 512), (z, z, z, z, 128, 64, 0, zero_k)])
+    torch.cuda.synchronize()
+    assert torch.equal(outs[1], m.gemm_fp4(*o2, 256, 512, 512))
+    assert torch.count_nonzero(outs[2]).item() == 0
