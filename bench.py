@@ -271,17 +271,24 @@ class Step:
         pin = lambda r, c: torch.empty(r, c, dtype=torch.bfloat16).pin_memory()
         self.e2e_host_out = [self.out_host, {"y": pin(M, N), "dx": pin(M, K), "dw": pin(N, K)}]
 
-    def launches_on(self, xs, outs, stream):
+    def launches_on(self, xs, outs, stream, grouped=True):
         m = self.m
         x, w, dy = xs
-        return [
+        y, dx, dw = outs
+        casts = [
             lambda: m.mxfp4_cast_dual(x, hadamard_col=True, out=self.qx, stream=stream),
             lambda: m.mxfp4_cast_dual(w, out=self.qw, stream=stream),
             lambda: m.mxfp4_cast_dual(dy, hadamard_col=True, out=self.qdy, stream=stream),
-            lambda: self.gemms_grouped(stream, outs),
+        ]
+        if grouped:
+            return casts + [lambda: self.gemms_grouped(stream, outs)]
+        return casts + [
+            lambda: m.gemm_fp4(self.qx[0], self.qx[1], self.qw[0], self.qw[1], M, N, K, c=y, stream=stream),
+            lambda: m.gemm_fp4(self.qdy[0], self.qdy[1], self.qw[2], self.qw[3], M, K, N, c=dx, stream=stream),
+            lambda: m.gemm_fp4(self.qdy[2], self.qdy[3], self.qx[2], self.qx[3], N, K, M, c=dw, stream=stream),
         ]
 
-    def run_e2e_pipelined(self, n_steps, streams, ev):
+    def run_e2e_pipelined(self, n_steps, streams, ev, grouped=True):
         """n_steps train steps from pinned host inputs to pinned host outputs.
 
         Every step copies its inputs host->device (copy-in stream), runs the
@@ -304,7 +311,7 @@ class Step:
             s_comp.wait_event(ev["in_ready"][b])
             if i >= 2:
                 s_comp.wait_event(ev["out_free"][b])       # step i-2's outputs have been downloaded
-            fs = self.launches_on(xs, outs, s_comp)
+            fs = self.launches_on(xs, outs, s_comp, grouped)
             for f in fs[:3]:
                 f()
             ev["in_free"][b].record(s_comp)
@@ -948,7 +955,8 @@ def main():
         step.e2e_buffers(dev)
         streams = (torch.cuda.Stream(device=dev), stream, torch.cuda.Stream(device=dev))
         ev = {k: [torch.cuda.Event(), torch.cuda.Event()] for k in ("in_ready", "in_free", "out_ready", "out_free")}
-        step.run_e2e_pipelined(2, streams, ev)  # warm-up
+        grouped = not args.separate_gemms
+        step.run_e2e_pipelined(2, streams, ev, grouped)  # warm-up
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
@@ -956,7 +964,7 @@ def main():
         e0.record(stream)
         for st in (streams[0], streams[2]):
             st.wait_event(e0)
-        step.run_e2e_pipelined(k_e2e, streams, ev)
+        step.run_e2e_pipelined(k_e2e, streams, ev, grouped)
         for st in (streams[0], streams[2]):
             stream.wait_event(st.record_event())
         e1.record(stream)

@@ -25,7 +25,7 @@ from dataclasses import dataclass
 
 import torch
 
-from . import gemm_fp4, gemm_fp4_cast_out, mxfp4_cast, mxfp4_cast_dual, scales_bytes
+from . import gemm_fp4, gemm_fp4_cast_out, gemm_fp4_grouped, mxfp4_cast, mxfp4_cast_dual, scales_bytes
 
 
 @dataclass
@@ -148,14 +148,16 @@ class _MXFP4LinearFn(torch.autograd.Function):
         dy = dy.contiguous()
         dy_q = ctx.grad_q.quantize(dy)
         stream = torch.cuda.current_stream(dy.device)
-        dx = dw = None
+        gemms = {}
         if ctx.needs_input_grad[0]:
             # dX[M,K] = dY[M,N] . W[N,K]: row(dY) against col(W), contraction over N
-            dx = gemm_fp4(dy_q.q_row, dy_q.sf_row, ctx.w_q.q_col, ctx.w_q.sf_col, M, K, N, stream=stream)
+            gemms["dx"] = (dy_q.q_row, dy_q.sf_row, ctx.w_q.q_col, ctx.w_q.sf_col, M, K, N)
         if ctx.needs_input_grad[1]:
             # dW[N,K] = dY^T . X: col(dY) against col(X), contraction over the tokens M
-            dw = gemm_fp4(dy_q.q_col, dy_q.sf_col, ctx.x_q.q_col, ctx.x_q.sf_col, N, K, M, stream=stream)
-        return dx, dw, None, None, None
+            gemms["dw"] = (dy_q.q_col, dy_q.sf_col, ctx.x_q.q_col, ctx.x_q.sf_col, N, K, M)
+        # both backward GEMMs in one launch
+        outs = dict(zip(gemms, gemm_fp4_grouped(gemms.values(), stream=stream))) if gemms else {}
+        return outs.get("dx"), outs.get("dw"), None, None, None
 
 
 def mxfp4_linear(x: torch.Tensor, w: torch.Tensor, w_q: MXFP4Tensor | None = None,
@@ -239,18 +241,25 @@ class _MXFP4StackFn(torch.autograd.Function):
         for i in reversed(range(L)):
             N, K = ctx.shapes[i]
             x_q, w_q = ctx.acts[i], ctx.w_qs[i]
+            if i == 0:
+                # the first layer: its wgrad and dgrad (bf16 dX) in one launch
+                gemms = {}
+                if ctx.needs_input_grad[2]:
+                    gemms["dw"] = (dy_q.q_col, dy_q.sf_col, x_q.q_col, x_q.sf_col, N, K, M)
+                if ctx.needs_input_grad[0]:
+                    gemms["dx"] = (dy_q.q_row, dy_q.sf_row, w_q.q_col, w_q.sf_col, M, K, N)
+                outs = dict(zip(gemms, gemm_fp4_grouped(gemms.values(), stream=stream))) if gemms else {}
+                dws[0], dx = outs.get("dw"), outs.get("dx")
+                break
             if ctx.needs_input_grad[2 + i]:
                 # dW_i[N,K] = dY_i^T . X_i, contraction over the tokens
                 dws[i] = gemm_fp4(dy_q.q_col, dy_q.sf_col, x_q.q_col, x_q.sf_col, N, K, M, stream=stream)
-            if i > 0:
-                # dX_i = dY_i . W_i is the grad_out of layer i-1: only its casts
-                nxt = MXFP4Tensor.empty(M, K, True, dy.device)
-                gemm_fp4_cast_out(dy_q.q_row, dy_q.sf_row, w_q.q_col, w_q.sf_col, M, K, N, hadamard_col=True,
-                                  out=(nxt.q_row, nxt.sf_row, nxt.q_col, nxt.sf_col), write_c=False,
-                                  stream=stream)
-                dy_q = nxt
-            elif ctx.needs_input_grad[0]:
-                dx = gemm_fp4(dy_q.q_row, dy_q.sf_row, w_q.q_col, w_q.sf_col, M, K, N, stream=stream)
+            # dX_i = dY_i . W_i is the grad_out of layer i-1: only its casts
+            nxt = MXFP4Tensor.empty(M, K, True, dy.device)
+            gemm_fp4_cast_out(dy_q.q_row, dy_q.sf_row, w_q.q_col, w_q.sf_col, M, K, N, hadamard_col=True,
+                              out=(nxt.q_row, nxt.sf_row, nxt.q_col, nxt.sf_col), write_c=False,
+                              stream=stream)
+            dy_q = nxt
         return (dx, None, *dws)
 
 
