@@ -40,8 +40,9 @@
 //     barrier (their own data has landed by then), so no relay hop;
 //   * warps 6-13: epilogue -- each warp reads 32 lanes x 128 columns of the
 //     accumulator into registers as bf16 pairs, frees tensor memory at once,
-//     then writes four 32 x 32 blocks through its own 64-byte-swizzled
-//     shared-memory buffer with TMA stores, so the global writes are
+//     then stages four 32 x 32 blocks in 64-byte-swizzled shared memory; the
+//     four warps of a 128-column half stage side by side and one of them
+//     writes each 128 x 32 block with a TMA store, so the global writes are
 //     whole-line and asynchronous while the next tile's MMAs run.
 // M and N tails come from the TMA out-of-bounds zero fill on loads and the
 // TMA clipping of stores; a K tail (K % 64 == 32) reads zero codes past K.
@@ -129,6 +130,22 @@ struct Fmt {
   static_assert(kRingBytes + kEpiBytes + kBarrierBytes <= kSmemBytes, "shared memory");
 };
 
+// Named barriers 1 and 2: the four epilogue warps of one 128-column half of
+// the tile (128 threads).  named_bar_and also returns the AND of `ok` over
+// them, so that the four warps leave the tile loop together or not at all.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool named_bar_and(int id, int count, bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(ok ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32) {
   uint32_t out;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
@@ -164,7 +181,7 @@ struct GroupTiles {
 // Tensor maps of a launch: operands, scales and C of each GEMM, and the
 // output-cast code maps (kCastOut instance, one GEMM).
 struct GemmMaps {
-  CUtensorMap a[kMaxGroup], b[kMaxGroup], sfa[kMaxGroup], sfb[kMaxGroup], c[kMaxGroup];
+  CUtensorMap a[kMaxGroup], b[kMaxGroup], sfa[kMaxGroup], sfb[kMaxGroup], c[kMaxGroup], c128[kMaxGroup];
   CUtensorMap qr, qc;
 };
 
@@ -439,7 +456,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = (warp - kFirstEpiWarp) >> 2;      // which 128-column half of the tile
     const uint32_t acc_empty_leader = map_to_cta(acc_empty, 0);
     const int ew = warp - kFirstEpiWarp;
-    const uint32_t out_buf = smem_u32(sOut + ew * kOutStageBytes);
+    // C staging: the plain kernel keeps the four lane quarters of a half in
+    // consecutive buffers (rows 0-127 of the half, in order) for one
+    // 128-row store per block; the output-cast instance, one buffer per warp
+    const int stage_idx = kCastOut ? ew : h * 4 + q;
+    const uint32_t out_buf = smem_u32(sOut + stage_idx * kOutStageBytes);
     // output cast: row-code block (32 rows x 64 bytes, 64-byte swizzle like
     // the C block) and column codes (128 column rows x 16 bytes)
     const uint32_t rq_buf = smem_u32(sOut + (kEpiWarps + ew) * kOutStageBytes);
@@ -454,7 +475,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g = tile_group(p, t, lt);
       const GroupTiles& G = p.g[g];
       tile_coords(lt, G.num_mt, G.num_nt, G.group_m, mt, nt);
-      if (!mbar_wait(acc_full, acc_phase, abort_flag, &g_device_status, p.wait_limit_ns)) break;
+      {
+        bool okw = mbar_wait(acc_full, acc_phase, abort_flag, &g_device_status, p.wait_limit_ns);
+        // the half's four warps meet at named barriers below: one that gave up
+        // takes the other three out of the loop with it
+        if constexpr (!kCastOut) okw = named_bar_and(1 + h, 128, okw);
+        if (!okw) break;
+      }
       tc_fence_after();
       // Read all 128 columns (4 x 32) as bf16 pairs, then release the accumulator.
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + h * 128;
@@ -482,68 +509,91 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive_cluster(acc_empty_leader);  // accumulator free for the next tile
       // Four 32 x 32 blocks: row `lane` is 64 bytes = four 16-byte chunks, chunk j
       // stored at j ^ ((row / 2) % 4) (the 64-byte swizzle), conflict-free.
+      if constexpr (!kCastOut) {
+        // The half's four warps stage block c side by side (128 rows x 32
+        // columns) and one thread stores it with a single TMA store: a quarter
+        // of the store operations of one store per warp (measured: dgrad and
+        // the other K = 4096-8192 shapes 2-3% faster, results unchanged).
+        const int32_t row_half = mt * kBM + static_cast<int32_t>(rank) * kRowsPerCta;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (lane == 0) bulk_wait_group_read0();  // the previous block has left the buffer
-        __syncwarp();
+        for (int c = 0; c < 4; ++c) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          sts128(out_buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16), pk[c * 16 + 4 * j],
-                 pk[c * 16 + 4 * j + 1], pk[c * 16 + 4 * j + 2], pk[c * 16 + 4 * j + 3]);
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) {
-          if (G.has_c)  // the cast-only form writes no bf16 C
-            tma_store_2d(&maps.c[g], sOut + ew * kOutStageBytes, col0 + c * 32, row0);
-          bulk_commit_group();
-        }
-        if constexpr (kCastOut) {
-          if (do_row) {  // block c of this lane's row, read back from the staged block
-            // (from shared memory rather than the packed registers: the cast then
-            // cannot be scheduled ahead of the accumulator release, and pk dies
-            // with the block stores -- measured 7-14% faster, no spills)
-            uint32_t w[16], q4[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint4 v = lds128(sOut + ew * kOutStageBytes + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4));
-              w[4 * j] = v.x;
-              w[4 * j + 1] = v.y;
-              w[4 * j + 2] = v.z;
-              w[4 * j + 3] = v.w;
-            }
-            BlockScale s;
-            if (!had_row) {
-              s = quantize_bf16_block(w, q4);
-            } else {
-              float y[32];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                y[2 * i] = __uint_as_float(w[i] << 16);
-                y[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-              }
-              s = quantize_hadamard_block(y, q4);
-            }
-            row_sf |= s.byte << (8 * c);
-            sts128(rq_buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), q4[0], q4[1], q4[2], q4[3]);
+          for (int j = 0; j < 4; ++j)
+            sts128(out_buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16), pk[c * 16 + 4 * j],
+                   pk[c * 16 + 4 * j + 1], pk[c * 16 + 4 * j + 2], pk[c * 16 + 4 * j + 3]);
+          fence_proxy_async_shared();
+          named_bar_sync(1 + h, 128);  // the half's 128 rows are staged
+          if (q == 0 && lane == 0) {
+            if (G.has_c) tma_store_2d(&maps.c128[g], sOut + h * 4 * kOutStageBytes, col0 + c * 32, row_half);
+            bulk_commit_group();
+            bulk_wait_group_read0();  // the store has read the staging buffer
           }
-          if (do_col) {  // column c * 32 + lane of the staged block: 32 rows
-            uint32_t q4[4];
-            const uint32_t cb = out_buf + (lane & 7) * 2;
-            auto elem = [&](int r) { return lds_u16(cb + r * 64 + (((lane >> 3) ^ ((r >> 1) & 3)) << 4)); };
-            BlockScale s;
-            if (!had_col) {
-              uint32_t w[16];  // rows 2i, 2i + 1 as one bf16 pair
+          named_bar_sync(1 + h, 128);  // buffer free for the next block
+        }
+      } else {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) w[i] = __byte_perm(elem(2 * i), elem(2 * i + 1), 0x5410);
-              s = quantize_bf16_block(w, q4);
-            } else {
-              float y[32];
+        for (int c = 0; c < 4; ++c) {
+          if (lane == 0) bulk_wait_group_read0();  // the previous block has left the buffer
+          __syncwarp();
 #pragma unroll
-              for (int r = 0; r < 32; ++r) y[r] = __uint_as_float(elem(r) << 16);
-              s = quantize_hadamard_block(y, q4);
+          for (int j = 0; j < 4; ++j)
+            sts128(out_buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16), pk[c * 16 + 4 * j],
+                   pk[c * 16 + 4 * j + 1], pk[c * 16 + 4 * j + 2], pk[c * 16 + 4 * j + 3]);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            if (G.has_c)  // the cast-only form writes no bf16 C
+              tma_store_2d(&maps.c[g], sOut + ew * kOutStageBytes, col0 + c * 32, row0);
+            bulk_commit_group();
+          }
+          if constexpr (kCastOut) {
+            if (do_row) {  // block c of this lane's row, read back from the staged block
+              // (from shared memory rather than the packed registers: the cast then
+              // cannot be scheduled ahead of the accumulator release, and pk dies
+              // with the block stores -- measured 7-14% faster, no spills)
+              uint32_t w[16], q4[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint4 v = lds128(sOut + ew * kOutStageBytes + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4));
+                w[4 * j] = v.x;
+                w[4 * j + 1] = v.y;
+                w[4 * j + 2] = v.z;
+                w[4 * j + 3] = v.w;
+              }
+              BlockScale s;
+              if (!had_row) {
+                s = quantize_bf16_block(w, q4);
+              } else {
+                float y[32];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  y[2 * i] = __uint_as_float(w[i] << 16);
+                  y[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+                }
+                s = quantize_hadamard_block(y, q4);
+              }
+              row_sf |= s.byte << (8 * c);
+              sts128(rq_buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), q4[0], q4[1], q4[2], q4[3]);
             }
-            sts128(cq_buf + (c * 32 + lane) * 16, q4[0], q4[1], q4[2], q4[3]);
-            if (sf_tiles_ok) p.sf_col[col_sf_tile + lane * 16 + c * 4 + q] = static_cast<uint8_t>(s.byte);
+            if (do_col) {  // column c * 32 + lane of the staged block: 32 rows
+              uint32_t q4[4];
+              const uint32_t cb = out_buf + (lane & 7) * 2;
+              auto elem = [&](int r) { return lds_u16(cb + r * 64 + (((lane >> 3) ^ ((r >> 1) & 3)) << 4)); };
+              BlockScale s;
+              if (!had_col) {
+                uint32_t w[16];  // rows 2i, 2i + 1 as one bf16 pair
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w[i] = __byte_perm(elem(2 * i), elem(2 * i + 1), 0x5410);
+                s = quantize_bf16_block(w, q4);
+              } else {
+                float y[32];
+#pragma unroll
+                for (int r = 0; r < 32; ++r) y[r] = __uint_as_float(elem(r) << 16);
+                s = quantize_hadamard_block(y, q4);
+              }
+              sts128(cq_buf + (c * 32 + lane) * 16, q4[0], q4[1], q4[2], q4[3]);
+              if (sf_tiles_ok) p.sf_col[col_sf_tile + lane * 16 + c * 4 + q] = static_cast<uint8_t>(s.byte);
+            }
           }
         }
       }
@@ -612,14 +662,14 @@ bool make_scale_pair_map(CUtensorMap* map, const uint8_t* base, int64_t row_tile
   return r == CUDA_SUCCESS;
 }
 
-// Output map: bf16 [M, N] with row pitch ldc elements, boxes of 32 rows x 32
-// columns (64 bytes, 64-byte swizzle); stores clip at M and N.
-bool make_bf16_out_map(CUtensorMap* map, uint16_t* base, int64_t M, int64_t N, int64_t ldc) {
+// Output map: bf16 [M, N] with row pitch ldc elements, boxes of box_rows rows
+// x 32 columns (64 bytes, 64-byte swizzle); stores clip at M and N.
+bool make_bf16_out_map(CUtensorMap* map, uint16_t* base, int64_t M, int64_t N, int64_t ldc, uint32_t box_rows) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * 2};
-  cuuint32_t box[2] = {32, 32};
+  cuuint32_t box[2] = {32, box_rows};
   cuuint32_t estrides[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estrides,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
@@ -760,7 +810,8 @@ cudaError_t launch_gemm_fmt(const GemmArgs* list, int count, cudaStream_t stream
                        CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_scale_pair_map(&maps.sfb[g], args.b_sf, (args.N + 127) / 128, ktiles128, 4 * F::kKTiles))
       return cudaErrorInvalidValue;
-    if (args.c != nullptr && !make_bf16_out_map(&maps.c[g], args.c, args.M, args.N, args.ldc))
+    if (args.c != nullptr && (!make_bf16_out_map(&maps.c[g], args.c, args.M, args.N, args.ldc, 32) ||
+                              !make_bf16_out_map(&maps.c128[g], args.c, args.M, args.N, args.ldc, 128)))
       return cudaErrorInvalidValue;
     GroupTiles& G = p.g[g];
     G.num_mt = static_cast<int>((args.M + kBM - 1) / kBM);
