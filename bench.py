@@ -914,6 +914,19 @@ def main():
             gev[i][1].record(stream)
     stream.synchronize()
     grouped_t = [a.elapsed_time(b) / 1e3 for a, b in gev]
+    # the three casts back to back on one stream, events only around the
+    # group: each cast's set-up overlaps the previous one's tail (programmatic
+    # dependent launch), as in a step; an event between two launches stops that
+    cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_prof)]
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int((0.005 + 2.0 * n_prof * host_per_step) * 2.2e9))
+        for i in range(n_prof):
+            cev[i][0].record(stream)
+            for _, f in step.launches(stream)[:3]:
+                f()
+            cev[i][1].record(stream)
+    stream.synchronize()
+    cast_chain_t = [a.elapsed_time(b) / 1e3 for a, b in cev]
     kinds = [k for k, _ in step.launches(stream)]
     per = [[evs[i][j][0].elapsed_time(evs[i][j][1]) / 1e3 for j in range(n_launch)] for i in range(n_prof)]
     gemm_t = [sum(p[j] for j in range(n_launch) if kinds[j] == "gemm") for p in per]
@@ -946,6 +959,10 @@ def main():
         "cast_gbs_all": cast_gbs,
         "cast_frac_of_hbm_measured": cast_gbs / peaks["hbm"],
         "cast_frac_of_8tbs": cast_gbs / 8000.0,
+        "casts_back_to_back_us": statistics.mean(cast_chain_t) * 1e6,
+        "casts_back_to_back_frac_of_hbm_measured": cast_bytes / statistics.mean(cast_chain_t) / 1e9 / peaks["hbm"],
+        "casts_what": "cast_us: each cast between its own event pair (no overlap with its neighbours); "
+                      "casts_back_to_back: the three in a row with events only around them",
     }
 
     # --------------------------------------------------------------- e2e leg (host buffers)
