@@ -287,3 +287,23 @@ def test_grouped_gemm_edge_cases(m):
     torch.cuda.synchronize()
     assert torch.equal(outs[1], m.gemm_fp4(*o2, 256, 512, 512))
     assert torch.count_nonzero(outs[2]).item() == 0
+
+
+def test_repeated_grouped_train_step_gemms_are_bit_identical(m):
+    # The grouped launch of the step's fwd, dgrad and wgrad (3 x 2.9e12 FLOP,
+    # GEMMs of different K in one ring), 20 times back to back: the epilogue's
+    # shared staging of a half's four warps, its named barriers and the one
+    # 128-row store per block must give the same bytes every time.
+    M, N, K = 8192, 4096, 14336
+    specs = [(M, N, K), (M, K, N), (N, K, M)]
+    ops = [rand_operands(a, b, c, seed=31 + i) for i, (a, b, c) in enumerate(specs)]
+    runs = []
+    for _ in range(20):
+        outs = [torch.empty(a, b, dtype=torch.bfloat16, device="cuda") for a, b, _ in specs]
+        m.gemm_fp4_grouped([(*o, a, b, c, out) for o, (a, b, c), out in zip(ops, specs, outs)])
+        runs.append(outs)
+    torch.cuda.synchronize()
+    assert m.device_status() == 0
+    for i, outs in enumerate(runs[1:], 1):
+        for j, (c, c0) in enumerate(zip(outs, runs[0])):
+            assert torch.equal(c, c0), f"launch {i}, GEMM {j} differs from launch 0"
