@@ -16,6 +16,12 @@
 //     within 24 MiB (measured at the Llama-3.1-8B down-projection shapes: 8
 //     row tiles for K = 14336, 32 for K = 4096, 16 for K = 8192, each 1-3%
 //     faster than the other two sizes);
+//   * grouped: one launch may carry up to four independent GEMMs (their
+//     tensor maps and tile counts in the kernel parameters), whose tiles are
+//     numbered one GEMM after another; every role decodes a tile index the
+//     same way, and the ring's stages run on across GEMMs of different K.
+//     A training step's fwd, dgrad and wgrad then leave one partial last wave
+//     instead of three (gemm_fp4_grouped; a gemm_fp4 call is the one-GEMM case);
 //   * warp 0: TMA producer in each CTA -- FP4 codes with the 128-byte swizzle
 //     (a 256-element K slab is one 128-byte swizzle row) and the 512-byte
 //     scale tiles, which the cast already writes in the tensor-memory copy
