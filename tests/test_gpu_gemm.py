@@ -307,3 +307,29 @@ def test_repeated_grouped_train_step_gemms_are_bit_identical(m):
     for i, outs in enumerate(runs[1:], 1):
         for j, (c, c0) in enumerate(zip(outs, runs[0])):
             assert torch.equal(c, c0), f"launch {i}, GEMM {j} differs from launch 0"
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_grouped_gemm_random_mixed_shapes(m, seed):
+    # Four GEMMs of ragged M and N and different K per launch (a single partial
+    # stage at K = 32, K tails of 32 past a 64-deep step, several stages), in
+    # random order: tiles of one GEMM follow another's in the same ring, and
+    # each result must equal its own gemm_fp4 call bit for bit.
+    rng = np.random.default_rng(100 + seed)
+    shapes = [(int(rng.integers(1, 700)), int(rng.integers(1, 700)), int(rng.choice([32, 64, 96, 160, 288, 544])))
+              for _ in range(4)]
+    ops = [rand_operands(M, N, K, seed=1000 * seed + i) for i, (M, N, K) in enumerate(shapes)]
+    # C with a pitch rounded up to 8 elements (ragged N, aligned rows)
+    out = lambda M, N: torch.empty(M, (N + 7) // 8 * 8, dtype=torch.bfloat16, device="cuda")[:, :N]
+    grouped = m.gemm_fp4_grouped([(*o, M, N, K, out(M, N)) for o, (M, N, K) in zip(ops, shapes)])
+    sep = [m.gemm_fp4(*o, M, N, K, c=out(M, N)) for o, (M, N, K) in zip(ops, shapes)]
+    torch.cuda.synchronize()
+    assert m.device_status() == 0
+    for (M, N, K), a, b in zip(shapes, sep, grouped):
+        assert torch.equal(a, b), f"{M}x{N}x{K}"
+    # and the first one against the oracle
+    M, N, K = shapes[0]
+    ca, sa, cb, sb = (t.cpu().numpy() for t in ops[0])
+    ref = oracle.gemm_mxfp4(ca, oracle.sf_tile_to_linear(sa, M, K // 32), cb,
+                            oracle.sf_tile_to_linear(sb, N, K // 32), nthreads=8)
+    assert_close(grouped[0].float().cpu().numpy().astype(np.float64), ref, f"grouped {M}x{N}x{K}")
