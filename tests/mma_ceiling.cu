@@ -1,7 +1,7 @@
 // MMA-only rate of the fifth-generation tensor cores on this GPU: back-to-back
 // tcgen05.mma issued by one elected lane, operands in zeroed shared memory,
 // no loads, cycles per instruction (clock64 around the issue loop and the
-// final commit).  This is the ceiling the block-scaled FP4 GEMM is judged
+// final commit).  This is the ceiling the block-scaled FP4 GEMM is measured
 // against: a 256 x 256 x 64 pair MMA of kind::mxf4 per N cycles.
 //
 // Test infrastructure (built and run by tests/test_gpu_mma_ceiling.py); it
