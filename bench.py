@@ -1042,8 +1042,9 @@ def main():
                                            "four launches (three casts, one gemm_fp4_grouped of fwd, dgrad and wgrad)")
                                         + ("" if args.serial_step else
                                            ", the casts side by side on three streams")),
-                       "per_kernel": f"{n_prof} eager steps of six launches, and {n_prof} eager grouped GEMM launches, "
-                                     "each enqueued behind a GPU sleep, an event pair per launch"},
+                       "per_kernel": f"{n_prof} eager steps of six launches, {n_prof} eager grouped GEMM launches and "
+                                     f"{n_prof} runs of the three casts back to back, each enqueued behind a GPU sleep, "
+                                     "an event pair per launch (per run for the casts back to back)"},
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
