@@ -333,3 +333,21 @@ def test_grouped_gemm_random_mixed_shapes(m, seed):
     ref = oracle.gemm_mxfp4(ca, oracle.sf_tile_to_linear(sa, M, K // 32), cb,
                             oracle.sf_tile_to_linear(sb, N, K // 32), nthreads=8)
     assert_close(grouped[0].float().cpu().numpy().astype(np.float64), ref, f"grouped {M}x{N}x{K}")
+
+
+def test_grouped_gemms_on_two_side_streams_at_once(m):
+    # two grouped launches enqueued on two non-default streams, free to run
+    # side by side: each result equal to its own gemm_fp4 call
+    shapes_a = [(1024, 2048, 4096), (2048, 1024, 1056)]
+    shapes_b = [(512, 3072, 2048), (3072, 512, 544), (256, 256, 64)]
+    ops_a = [rand_operands(M, N, K, seed=70 + i) for i, (M, N, K) in enumerate(shapes_a)]
+    ops_b = [rand_operands(M, N, K, seed=80 + i) for i, (M, N, K) in enumerate(shapes_b)]
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    ga = m.gemm_fp4_grouped([(*o, M, N, K) for o, (M, N, K) in zip(ops_a, shapes_a)], stream=s1)
+    gb = m.gemm_fp4_grouped([(*o, M, N, K) for o, (M, N, K) in zip(ops_b, shapes_b)], stream=s2)
+    torch.cuda.synchronize()
+    assert m.device_status() == 0
+    for ops, shapes, got in ((ops_a, shapes_a, ga), (ops_b, shapes_b, gb)):
+        for o, (M, N, K), c in zip(ops, shapes, got):
+            assert torch.equal(c, m.gemm_fp4(*o, M, N, K)), f"{M}x{N}x{K}"
