@@ -350,13 +350,17 @@ def host_link_rates(step, streams, dev, reps=5):
                 hout[name].copy_(src, non_blocking=True)
 
     def timed(fns):
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
+        # the best of `reps` synchronized repetitions: a copy floor, so a slow
+        # first use (or a neighbour's traffic) must not raise it
+        best = float("inf")
         for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
             for f in fns:
                 f()
-        torch.cuda.synchronize()
-        return (time.perf_counter() - t0) / reps
+            torch.cuda.synchronize()
+            best = min(best, time.perf_counter() - t0)
+        return best
 
     up(), down()
     t_up, t_down, t_both = timed([up]), timed([down]), timed([up, down])
@@ -365,8 +369,9 @@ def host_link_rates(step, streams, dev, reps=5):
             "both_directions_gbs": (bi + bo) / t_both / 1e9, "copy_floor_ms_per_step": t_both * 1e3,
             "upload_ms": t_up * 1e3, "download_ms": t_down * 1e3,
             "cuda_device_max_connections": os.environ.get("CUDA_DEVICE_MAX_CONNECTIONS", "unset (8)"),
-            "what": "pinned copies of the step's inputs (H2D) and outputs (D2H), alone and both at once; "
-                    "copy_floor_ms_per_step is the time of one step's copies with no compute"}
+            "what": "pinned copies of the step's inputs (H2D) and outputs (D2H), alone and both at once, "
+                    f"best of {reps} synchronized repetitions each; copy_floor_ms_per_step is the time of one "
+                    "step's copies with no compute"}
 
 
 # ----------------------------------------------------------------------------- layer and FP8 legs
