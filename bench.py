@@ -1018,7 +1018,7 @@ def main():
             raise RuntimeError("device status word set in the layer leg")
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:  # the oracle baseline: one GPU only
         nthreads = cpu_threads()
         est, spent, desc = oracle_sample(8192, 256, 1536, nthreads)  # ~10-15 s of CPU work
         cpu = {"value": STEP_FLOPS / est / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
