@@ -545,9 +545,33 @@ def gemm_shapes_leg(m, dev, stream, iters=10):
         flop_total += flop
         time_total += t
         del a, b, a_sf, b_sf, c
+    # each 70B layer's fwd, dgrad and wgrad in one gemm_fp4_grouped launch
+    grouped, gflop, gtime = {}, 0.0, 0.0
+    for name in ("llama70b_qkv", "llama70b_o", "llama70b_gate_up", "llama70b_down"):
+        M_, N_, K_, _ = synth.LLAMA_SHAPES[name]
+        specs = [(M_, N_, K_), (M_, K_, N_), (N_, K_, M_)]
+        descs = []
+        for mo, no, kc in specs:
+            descs.append((rnd(mo * kc // 2), sf(mo, kc), rnd(no * kc // 2), sf(no, kc), mo, no, kc,
+                          torch.empty(mo, no, dtype=torch.bfloat16, device=dev)))
+        t = time_loop(lambda: m.gemm_fp4_grouped(descs, stream=stream), iters, 3, stream)
+
+        def three():
+            for d in descs:
+                m.gemm_fp4(*d[:7], c=d[7], stream=stream)
+        t_sep = time_loop(three, iters, 3, stream)
+        flop = sum(2.0 * mo * no * kc for mo, no, kc in specs)
+        grouped[name] = {"tflops": flop / t / 1e12, "us": t * 1e6, "separate_us": t_sep * 1e6,
+                         "separate_tflops": flop / t_sep / 1e12}
+        gflop += flop
+        gtime += t
+        del descs
     return {"unit": "TFLOP/s", "gemms": out, "flop_weighted_tflops": flop_total / time_total / 1e12,
+            "grouped_70b_layers": grouped, "grouped_flop_weighted_tflops": gflop / gtime / 1e12,
             "what": "gemm_fp4 at the 8B gate/up forward and the 70B layer shapes (M = 8192 tokens), "
-                    "CUDA events, back to back"}
+                    "CUDA events, back to back; grouped_70b_layers: each 70B layer's fwd, dgrad and wgrad as "
+                    "one gemm_fp4_grouped launch, against the same three as gemm_fp4 launches in a row "
+                    "(both repeated, so both see the same L2 state)"}
 
 
 def stack_leg(dev, stream, iters=10):
