@@ -178,3 +178,20 @@ def test_same_stream_ordering(m):
     q, _ = m.mxfp4_cast(x, stream=s)
     s.synchronize()
     assert np.array_equal(q.cpu().numpy(), oracle.cast_rows(bf16_bits(a))[0])
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_shapes_and_flags(m, seed):
+    # Seeded random shapes (rows and columns multiples of 32, from one slab to
+    # a few dozen tiles, so the grid's whole rounds, the slab-by-slab tail and
+    # the tile-staged and direct scale paths all occur), random Hadamard flags
+    # and scale layout, activations with outliers: every code and scale byte
+    # equal to the oracle's.
+    rng = np.random.default_rng(500 + seed)
+    R = 32 * int(rng.integers(1, 80))
+    C = 32 * int(rng.integers(1, 80))
+    had_row, had_col, linear = (bool(v) for v in rng.integers(0, 2, size=3))
+    x = synth.with_outliers(synth.normal_bf16((R, C), float(rng.choice([1e-3, 0.02, 1.0])), seed=600 + seed),
+                            frac=0.001)
+    check_dual(m, x, had_row, had_col, linear)
+    check_row(m, x, had_row, linear)
