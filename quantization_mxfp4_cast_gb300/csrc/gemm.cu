@@ -22,12 +22,15 @@
 //     same way, and the ring's stages run on across GEMMs of different K.
 //     A training step's fwd, dgrad and wgrad then leave one partial last wave
 //     instead of three (gemm_fp4_grouped; a gemm_fp4 call is the one-GEMM case);
-//   * warp 0: TMA producer in each CTA -- FP4 codes with the 128-byte swizzle
-//     (a 256-element K slab is one 128-byte swizzle row) and the 512-byte
-//     scale tiles, which the cast already writes in the tensor-memory copy
-//     layout (B's two 128-row tiles in one 3-D box), into a 6-stage
-//     shared-memory ring (measured: 4 stages are 11% slower; the 5-stage ring
-//     of the output-cast instance is 4-6% slower with no cast work);
+//   * warps 0 and 14: TMA producers in each CTA -- warp 0 the FP4 codes with
+//     the 128-byte swizzle (a 256-element K slab is one 128-byte swizzle row),
+//     warp 14 the 512-byte scale tiles, which the cast already writes in the
+//     tensor-memory copy layout (B's two 128-row tiles in one 3-D box), into
+//     a 6-stage shared-memory ring (measured: 4 stages are 11% slower; the
+//     5-stage ring of the output-cast instance is 4-6% slower with no cast
+//     work).  The ring, not the tensor pipe, sets the pace: a stage's release
+//     (the commit of its MMAs) comes ~1,000-2,000 cycles after they are
+//     issued, so every link from release to refill counts;
 //   * warps 2-5, in each CTA: scale stagers -- each takes one 32-lane quarter
 //     of tensor memory and writes the stage's A and B scales there with
 //     tcgen05.st (the layout the block-scaled MMA reads: lane i of every
@@ -38,12 +41,11 @@
 //   * warp 1 of the first CTA: tensor-core issuer -- four
 //     tcgen05.mma.kind::mxf4 per stage (K = 64, two UE8M0 scales per row each)
 //     update a 256 x 256 fp32 accumulator (128 lanes x 256 columns in each
-//     SM); tcgen05.commit multicasts the stage release to both CTAs.  The
-//     warp stays converged and one elected lane issues, with the operand
-//     descriptors precomputed (the issue rate of this one warp bounds the
-//     whole GEMM: ~55 cycles per MMA this way, ~93 from a lone lane).  The
-//     stagers of both CTAs report "stage ready" straight to the first CTA's
-//     barrier (their own data has landed by then), so no relay hop;
+//     SM); tcgen05.commit multicasts the stage release to both CTAs.  One
+//     elected lane runs the whole loop, stepping the operand descriptors
+//     from stage to stage (~160 cycles from "scales ready" to the commit).
+//     The stagers of both CTAs report "stage ready" straight to the first
+//     CTA's barrier (their own data has landed by then), so no relay hop;
 //   * warps 6-13: epilogue -- each warp reads 32 lanes x 128 columns of the
 //     accumulator into registers as bf16 pairs, frees tensor memory at once,
 //     then stages four 32 x 32 blocks in 64-byte-swizzled shared memory; the
@@ -92,7 +94,8 @@ constexpr int64_t kRasterPanelBytes = int64_t(24) << 20;  // A panel of one rast
 constexpr int kScaleWarps = 4;   // warps 2-5
 constexpr int kEpiWarps = 8;     // warps 6-13
 constexpr int kFirstEpiWarp = 2 + kScaleWarps;
-constexpr int kThreads = 32 * (2 + kScaleWarps + kEpiWarps);
+constexpr int kSfLoadWarp = kFirstEpiWarp + kEpiWarps;  // warp 14: the scale-tile loads
+constexpr int kThreads = 32 * (kSfLoadWarp + 1);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;
 constexpr uint32_t kSfCol0 = kBN;
@@ -296,8 +299,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pair = static_cast<int>(blockIdx.x >> 1);
   const int num_pairs = static_cast<int>(gridDim.x >> 1);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer (both CTAs)
+  if (warp == 0 || warp == kSfLoadWarp) {
+    // ------------------------------------------------------------ producers (both CTAs)
+    // Warp 0 arms each stage's barrier for all its bytes and loads the A and
+    // B codes; warp 14 loads the two scale boxes of the same stage once the
+    // stage is free (its bytes may land before the arming: the barrier's
+    // transaction count runs below zero until then).  Two threads issuing
+    // the four loads side by side, instead of one issuing them in turn,
+    // shorten the path from a stage's release to its refill (measured: 4-9%
+    // faster GEMMs at the Llama shapes).
+    const bool code_loads = warp == 0;
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
@@ -315,15 +326,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const int kg0 = kt * F::kKTiles;
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
-          tma_load_2d(sA + stage * kAStage, &maps.a[g], &full[stage], kt * kBKBytes, a_row);
-          tma_load_2d(sB + stage * kBStage, &maps.b[g], &full[stage], kt * kBKBytes, b_row);
-          tma_load_2d(sSfa + stage * kSfaStage, &maps.sfa[g], &full[stage], 0,
-                      (a_rt * G.ktiles128 + kg0) * 4);
-          // both 128-row scale tiles of B in one box (measured: 4-7% faster
-          // than two 2-D loads)
-          tma_load_3d(sSfb + stage * kSfbStage, &maps.sfb[g], &full[stage], 0, kg0 * 4, nt * 2);
+          if (code_loads) {
+            mbar_arrive_expect_tx(&full[stage], kStageBytes);
+            tma_load_2d(sA + stage * kAStage, &maps.a[g], &full[stage], kt * kBKBytes, a_row);
+            tma_load_2d(sB + stage * kBStage, &maps.b[g], &full[stage], kt * kBKBytes, b_row);
+          } else {
+            const int kg0 = kt * F::kKTiles;
+            tma_load_2d(sSfa + stage * kSfaStage, &maps.sfa[g], &full[stage], 0,
+                        (a_rt * G.ktiles128 + kg0) * 4);
+            // both 128-row scale tiles of B in one box (measured: 4-7% faster
+            // than two 2-D loads)
+            tma_load_3d(sSfb + stage * kSfbStage, &maps.sfb[g], &full[stage], 0, kg0 * 4, nt * 2);
+          }
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -333,7 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Every load issued has landed before the CTA may end: the stagers wait
       // for all of them unless a wait gave up.  The last load into a stage
-      // completes the phase its index gives; nothing follows it.
+      // completes the phase its index gives; nothing follows it.  Each
+      // producer waits for the stages it loaded into; where a wait gave up
+      // first, the other producer may not have armed or filled such a stage,
+      // and this wait then runs out its limit, long after its own loads landed.
       volatile int keep_waiting = 0;  // not the CTA's abort flag: this wait must run its course
       for (int s = 0; s < kStages && s < issued; ++s) {
         const int last = s + ((issued - 1 - s) / kStages) * kStages;
@@ -343,35 +360,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (leader) {
       // ------------------------------------------------------------ MMA issuer
-      // The whole warp runs the loop (so the descriptors stay warp-uniform)
-      // and one elected lane issues each stage's MMAs and the commit.
-      // Measured: issuing from a lone lane of a diverged warp cost ~93 cycles
-      // per tcgen05.mma and left the tensor pipe idle half the time; from a
-      // converged warp with precomputed descriptors it is ~55 cycles.
-      uint32_t stage = 0, phase = 0, acc_phase = 0;
-      bool ok = true;
-      const uint64_t adesc0 = make_smem_desc(smem_u32(sA), 16, 1024, 2);
-      const uint64_t bdesc0 = make_smem_desc(smem_u32(sB), 16, 1024, 2);
-      for (int t = pair; ok && t < num_tiles; t += num_pairs) {
-        int lt;
-        const GroupTiles& G = p.g[tile_group(p, t, lt)];
-        ok = mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, &g_device_status, p.wait_limit_ns);
-        if (!__all_sync(0xFFFFFFFFu, ok)) break;
-        tc_fence_after();
-        for (int kt = 0; kt < G.num_kt; ++kt) {
-          ok = mbar_wait(&sf_ready[stage], phase, abort_flag, &g_device_status, p.wait_limit_ns);
-          if (!__all_sync(0xFFFFFFFFu, ok)) {
-            ok = false;
-            break;
-          }
+      // One elected lane runs the whole loop: the waits, four MMAs and the
+      // commit per stage, with the descriptors stepped from stage to stage.
+      // Measured: ~160 cycles from a stage's scales being ready to its
+      // commit, against ~300 with the whole warp running the loop and
+      // electing a lane per stage (a vote, an elect and a re-convergence
+      // each time); the GEMMs at the Llama shapes ran 1-3% faster.
+      if (elect_one_sync()) {
+        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        bool ok = true;
+        // Descriptor start addresses are in 16-byte units: a stage is
+        // kAStage / 16 further, a 64-deep k-step 32 bytes (2 units).
+        const uint64_t adesc0 = make_smem_desc(smem_u32(sA), 16, 1024, 2);
+        const uint64_t bdesc0 = make_smem_desc(smem_u32(sB), 16, 1024, 2);
+        uint64_t a_d = adesc0, b_d = bdesc0;
+        uint32_t sf_col = tmem_base + kSfCol0;
+        for (int t = pair; ok && t < num_tiles; t += num_pairs) {
+          int lt;
+          const GroupTiles& G = p.g[tile_group(p, t, lt)];
+          ok = mbar_wait(acc_empty, acc_phase ^ 1u, abort_flag, &g_device_status, p.wait_limit_ns);
+          if (!ok) break;
           tc_fence_after();
-          // Descriptor start addresses are in 16-byte units: a stage is
-          // kAStage / 16 further, a 64-deep k-step 32 bytes (2 units).
-          const uint64_t a_d = adesc0 + ((stage * kAStage) >> 4);
-          const uint64_t b_d = bdesc0 + ((stage * kBStage) >> 4);
-          const uint32_t sf_col = tmem_base + kSfCol0 + stage * kSfStageCols;
-          const int nks = kt + 1 < G.num_kt ? 4 : G.last_nks;
-          if (elect_one_sync()) {
+          for (int kt = 0; kt < G.num_kt; ++kt) {
+            ok = mbar_wait(&sf_ready[stage], phase, abort_flag, &g_device_status, p.wait_limit_ns);
+            if (!ok) break;
+            tc_fence_after();
+            const int nks = kt + 1 < G.num_kt ? 4 : G.last_nks;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               if (ks < nks) {
@@ -388,26 +402,30 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
             tc_commit_pair(&empty[stage], 0x3);
+            a_d += kAStage >> 4;
+            b_d += kBStage >> 4;
+            sf_col += kSfStageCols;
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+              a_d = adesc0;
+              b_d = bdesc0;
+              sf_col = tmem_base + kSfCol0;
+            }
           }
-          __syncwarp();
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          if (!ok) break;
+          tc_commit_pair(acc_full, 0x3);
+          acc_phase ^= 1u;
         }
-        if (!ok) break;
-        if (elect_one_sync()) tc_commit_pair(acc_full, 0x3);
-        __syncwarp();
-        acc_phase ^= 1u;
+        // Every MMA issued (they read both CTAs' shared memory and write their
+        // tensor memory) has completed before the teardown: already so on the
+        // normal path, not when a wait gave up mid-tile.
+        tc_commit_pair(mma_drain, 0x1);
+        volatile int keep_waiting = 0;
+        mbar_wait(mma_drain, 0, &keep_waiting, &g_device_status, p.wait_limit_ns);
+        tc_fence_after();
       }
-      // Every MMA issued (they read both CTAs' shared memory and write their
-      // tensor memory) has completed before the teardown: already so on the
-      // normal path, not when a wait gave up mid-tile.
-      if (elect_one_sync()) tc_commit_pair(mma_drain, 0x1);
       __syncwarp();
-      volatile int keep_waiting = 0;
-      mbar_wait(mma_drain, 0, &keep_waiting, &g_device_status, p.wait_limit_ns);
-      tc_fence_after();
     }
   } else if (warp < kFirstEpiWarp) {
     // ------------------------------------------------------------ scale stagers (both CTAs)
