@@ -348,13 +348,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Every load issued has landed before the CTA may end: the stagers wait
       // for all of them unless a wait gave up.  The last load into a stage
       // completes the phase its index gives; nothing follows it.  Each
-      // producer waits for the stages it loaded into; where a wait gave up
-      // first, the other producer may not have armed or filled such a stage,
-      // and this wait then runs out its limit, long after its own loads landed.
+      // producer waits for the stages it loaded into.  Where a wait gave up
+      // first, the other producer may not have armed or filled such a stage:
+      // that wait runs out its limit, long after this producer's own loads
+      // landed, and the ones after it are skipped.
       volatile int keep_waiting = 0;  // not the CTA's abort flag: this wait must run its course
       for (int s = 0; s < kStages && s < issued; ++s) {
         const int last = s + ((issued - 1 - s) / kStages) * kStages;
-        mbar_wait(&full[s], (last / kStages) & 1, &keep_waiting, &g_device_status, p.wait_limit_ns);
+        if (!mbar_wait(&full[s], (last / kStages) & 1, &keep_waiting, &g_device_status, p.wait_limit_ns)) break;
       }
     }
   } else if (warp == 1) {
