@@ -17,20 +17,26 @@
 //     blocks -- so no warp waits for another one to finish a tile;
 //   * one persistent CTA per SM owns the 128 x 128 tiles blockIdx.x + k *
 //     gridDim.x.  A producer thread streams their slabs with TMA (two 32 x 64
-//     boxes, 128-byte swizzle, zero fill past the edges) into a ring of 24
-//     slots; 15 consumer warps take the slabs in order from a shared counter
+//     boxes, 128-byte swizzle, zero fill past the edges) into a ring of 20
+//     slots (measured: 24 slots leave no room for the column-code buffers
+//     below, 16 are 4-8% slower); 15 consumer warps take the slabs in order from a shared counter
 //     as they become free, so the four slabs of a tile are quantized side by
 //     side (balanced to within one slab per SM, with loads in flight beyond the
 //     slabs being quantized).  A slot's sequence word tells a consumer when
 //     the producer has claimed the slot for its slab (and publishes the
 //     slab's coordinates), so no consumer waits on a barrier phase that
 //     belongs to an earlier use of the slot;
-//   * the four 16-byte column-code pieces of a tile's column are written by
-//     those four warps at nearly the same time (measured: when the pieces of
-//     a 64-byte run came from different SMs at different times, the stores
-//     took ~2.5x as long), and a tile's two 512-byte scale tiles are
-//     assembled in shared memory and written whole by the warp that finishes
-//     the tile's last slab;
+//   * a tile's column codes (128 columns x 64 bytes: four 16-byte pieces per
+//     column, one from each slab's warp) and its two 512-byte scale tiles are
+//     assembled in shared memory; the warp that finishes the tile's last slab
+//     writes the codes with one TMA store (64-byte swizzle, clipped at the
+//     tensor's edges) and the scale tiles whole.  Each warp storing its 16-byte
+//     pieces straight to memory, 32 columns apart per instruction, made the
+//     dual cast's column output the bottleneck (measured: with no arithmetic
+//     at all the old kernel ran as fast as the real one; staging the pieces
+//     took X[8192, 14336] from 5.1 to 6.4 TB/s, 0.94 of the copy rate).  A
+//     partial last round of tiles, dealt out slab by slab over the CTAs, and
+//     the linear scale layout keep the direct stores;
 //   * row blocks: lane l takes row 8i + l % 8 (i = 0..3), block l / 8, read as
 //     four 16-byte chunks (conflict-free under the swizzle); a store
 //     instruction writes 8 rows x 64 contiguous bytes;
@@ -62,13 +68,17 @@ constexpr int kSlabRows = 32;
 constexpr int kSlabCols = 128;
 constexpr int kHalfBytes = kSlabRows * 128;  // one 64-column half: 32 rows x 128 bytes
 constexpr int kSlabBytes = 2 * kHalfBytes;   // 8 KB
-constexpr int kStages = 24;                  // ring slots
+constexpr int kStages = 20;                  // ring slots
 constexpr int kConsumerWarps = 15;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + the producer warp
-constexpr int kSfBufs = 12;                  // scale-tile staging buffers (tiles in progress)
+constexpr int kSfBufs = 8;                   // scale-tile staging buffers (tiles in progress)
+constexpr int kCqBufs = 6;                   // column-code staging buffers (tiles in progress)
+constexpr int kCqBytes = 128 * 64;           // a tile's column codes: 128 columns x 64 bytes
 constexpr int kSfStageBytes = 2 * 512;       // one tile's row and column scale tiles
-constexpr int kBarrierBytes = 2 * kStages * 8 + 3 * kStages * 4 + 2 * kSfBufs * 4 + 16;
-constexpr int kCastSmemBytes = kStages * kSlabBytes + kSfBufs * kSfStageBytes + kBarrierBytes + 1024;
+constexpr int kBarrierBytes = 2 * kStages * 8 + 3 * kStages * 4 + 2 * kSfBufs * 4 + kCqBufs * 4 + 16;
+constexpr int kCastSmemBytes =
+    kStages * kSlabBytes + kSfBufs * kSfStageBytes + kCqBufs * kCqBytes + kBarrierBytes + 1024;
+static_assert(kCastSmemBytes <= 232448, "shared memory");
 static_assert(kStages % 4 == 0, "a tile's four slabs take four consecutive ring slots");
 constexpr uint32_t kNoSlab = 0xFFFFFFFFu;
 
@@ -139,7 +149,8 @@ __device__ __forceinline__ bool wait_word(const uint32_t* p, uint32_t want, vola
 // one slab of every other's; a tail slab writes its scale bytes directly.
 template <bool kRow, bool kCol, bool kFp8, bool kHadRow, bool kHadCol>
 __global__ void __launch_bounds__(kThreads, 1)
-    cast_kernel(const __grid_constant__ CUtensorMap tmX, const CastArgs args, int col_tiles,
+    cast_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmQc,
+                const CastArgs args, int col_tiles,
                 int row_tiles128, int num_tiles, int* status) {
   static_assert(!(kFp8 && kRow), "MXFP8 is produced column-wise only");
   extern __shared__ uint8_t smem_raw[];
@@ -147,14 +158,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* ring = smem;
   uint8_t* sf_stage = smem + kStages * kSlabBytes;  // [kSfBufs][row tile, column tile]
-  uint64_t* full = reinterpret_cast<uint64_t*>(sf_stage + kSfBufs * kSfStageBytes);
+  uint8_t* cq_stage = sf_stage + kSfBufs * kSfStageBytes;  // [kCqBufs][128 columns x 64 B], 64-byte swizzle
+  uint64_t* full = reinterpret_cast<uint64_t*>(cq_stage + kCqBufs * kCqBytes);
   uint64_t* empty = full + kStages;
   uint32_t* seq = reinterpret_cast<uint32_t*>(empty + kStages);  // local slab that owns each slot
   uint32_t* slot_rb = seq + kStages;                                // its 32-row block
   uint32_t* slot_ct = slot_rb + kStages;                            // its 128-column tile
   uint32_t* sf_free = slot_ct + kStages;   // staging buffer b is free for local tile sf_free[b]
   int* tile_done = reinterpret_cast<int*>(sf_free + kSfBufs);      // slabs of the tile in b finished
-  int* counter = tile_done + kSfBufs;                                // next local slab to hand out
+  // column-code buffer b is free for local tile cq_free[b]
+  uint32_t* cq_free = reinterpret_cast<uint32_t*>(tile_done + kSfBufs);
+  int* counter = reinterpret_cast<int*>(cq_free + kCqBufs);          // next local slab to hand out
   volatile int* abort_flag = counter + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -178,7 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (t < kStages + kSfBufs) {
       sf_free[t - kStages] = static_cast<uint32_t>(t - kStages);
       tile_done[t - kStages] = 0;
-    } else if (t == kStages + kSfBufs) {
+    } else if (t < kStages + kSfBufs + kCqBufs) {
+      cq_free[t - kStages - kSfBufs] = static_cast<uint32_t>(t - kStages - kSfBufs);
+    } else if (t == kStages + kSfBufs + kCqBufs) {
       *counter = 0;
       *abort_flag = 0;
     }
@@ -271,6 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sf_col_stage = staged ? sf_row_stage + 512
                                    : args.sf_col + (static_cast<size_t>(ct) * row_tiles128 + (rb >> 2)) * 512;
     if (staged && !wait_word(&sf_free[sfb], static_cast<uint32_t>(i >> 2), abort_flag, status)) break;
+    // column codes: assembled per whole tile in shared memory (64 contiguous
+    // bytes per column) and written by one TMA store
+    const bool cq_staged = staged && kCol && !kFp8;
+    const int cqb = (i >> 2) % kCqBufs;
+    if (cq_staged && !wait_word(&cq_free[cqb], static_cast<uint32_t>(i >> 2), abort_flag, status)) break;
     if (!mbar_wait(&full[slot], (i / kStages) & 1, abort_flag, status)) break;
     const uint8_t* tile = ring + slot * kSlabBytes;
     const int64_t c0 = static_cast<int64_t>(ct) * kSlabCols;
@@ -398,7 +419,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const BlockScale& sc = half ? sb : sa;
           const uint32_t* cw = half ? cb : ca;
           const int64_t gcol = c0 + c;
-          if (gcol < cols && rows_ok) {
+          if (cq_staged) {
+            // column c's 16 bytes of this slab (slab j = rb % 4 of the tile), chunk j of
+            // the column's 64-byte row under the 64-byte swizzle the TMA store undoes
+            const uint32_t dst =
+                smem_u32(cq_stage + cqb * kCqBytes) + c * 64 + (((rb & 3) ^ ((c >> 1) & 3)) << 4);
+            sts128(dst, cw[0], cw[1], cw[2], cw[3]);
+          } else if (gcol < cols && rows_ok) {
             // codes of T^T: [cols, rows] bytes (MXFP8) or [cols, rows / 2] (MXFP4)
             uint4* dst = reinterpret_cast<uint4*>(args.q_col + (gcol * rows + r0) / (kFp8 ? 1 : 2));
             dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
@@ -412,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (cq_staged) fence_proxy_async_shared();  // this lane's column codes, before the TMA store reads them
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);  // the slot may be refilled
     if (staged) {
@@ -430,6 +458,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kCol)
           reinterpret_cast<uint4*>(args.sf_col + (tile_x * row_tiles128 + tile_y) * 512)[lane] =
               reinterpret_cast<const uint4*>(sf_col_stage)[lane];
+        if (cq_staged && lane == 0) {
+          // the tile's column codes: 128 columns x 64 bytes (rows past the end
+          // and columns past cols are clipped by the store)
+          tma_store_2d(&tmQc, cq_stage + cqb * kCqBytes, static_cast<int32_t>(tile_y * 64),
+                       static_cast<int32_t>(tile_x * 128));
+          bulk_commit_group();
+          bulk_wait_group_read0();  // the buffer has been read
+          st_release_shared(&cq_free[cqb], static_cast<uint32_t>((i >> 2) + kCqBufs));
+        }
         __syncwarp();
         if (lane == 0) {
           tile_done[sfb] = 0;
@@ -438,11 +475,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  if (lane == 0) bulk_wait_group0();  // this warp's column-code stores are complete
 }
 
 template <bool kRow, bool kCol, bool kFp8, bool kHadRow, bool kHadCol>
-cudaError_t launch_cast_t(const CUtensorMap& tm, const CastArgs& args, int col_tiles, int row_tiles128,
-                          int num_tiles, int dev, cudaStream_t stream) {
+cudaError_t launch_cast_t(const CUtensorMap& tm, const CUtensorMap& tm_qc, const CastArgs& args, int col_tiles,
+                          int row_tiles128, int num_tiles, int dev, cudaStream_t stream) {
   auto kernel = cast_kernel<kRow, kCol, kFp8, kHadRow, kHadCol>;
   static std::atomic<int> ctas[64];  // resident CTAs on the whole GPU, per device
   int grid = (dev >= 0 && dev < 64) ? ctas[dev].load(std::memory_order_relaxed) : 0;
@@ -471,25 +509,25 @@ cudaError_t launch_cast_t(const CUtensorMap& tm, const CastArgs& args, int col_t
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, tm, args, col_tiles, row_tiles128, num_tiles, status);
+  return cudaLaunchKernelEx(&cfg, kernel, tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, status);
 }
 
 template <bool kRow, bool kCol, bool kFp8>
-cudaError_t launch_had(const CUtensorMap& tm, const CastArgs& args, int col_tiles, int row_tiles128,
-                       int num_tiles, int dev, cudaStream_t stream) {
+cudaError_t launch_had(const CUtensorMap& tm, const CUtensorMap& tm_qc, const CastArgs& args, int col_tiles,
+                       int row_tiles128, int num_tiles, int dev, cudaStream_t stream) {
   const bool hr = kRow && (args.flags & kFlagHadamardRow) != 0;
   const bool hc = kCol && (args.flags & kFlagHadamardCol) != 0;
   if constexpr (kRow && kCol) {
-    if (hr && hc) return launch_cast_t<true, true, kFp8, true, true>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
-    if (hr) return launch_cast_t<true, true, kFp8, true, false>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
-    if (hc) return launch_cast_t<true, true, kFp8, false, true>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
-    return launch_cast_t<true, true, kFp8, false, false>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    if (hr && hc) return launch_cast_t<true, true, kFp8, true, true>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    if (hr) return launch_cast_t<true, true, kFp8, true, false>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    if (hc) return launch_cast_t<true, true, kFp8, false, true>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    return launch_cast_t<true, true, kFp8, false, false>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
   } else if constexpr (kRow) {
-    if (hr) return launch_cast_t<true, false, kFp8, true, false>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
-    return launch_cast_t<true, false, kFp8, false, false>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    if (hr) return launch_cast_t<true, false, kFp8, true, false>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    return launch_cast_t<true, false, kFp8, false, false>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
   } else {
-    if (hc) return launch_cast_t<false, true, kFp8, false, true>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
-    return launch_cast_t<false, true, kFp8, false, false>(tm, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    if (hc) return launch_cast_t<false, true, kFp8, false, true>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    return launch_cast_t<false, true, kFp8, false, false>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
   }
 }
 
@@ -508,6 +546,18 @@ cudaError_t launch_cast(const CastArgs& args, cudaStream_t stream) {
          estrides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  // column codes [cols, rows / 2] (MXFP4), stored a tile (128 columns x 64
+  // bytes) at a time from a 64-byte-swizzled staging buffer
+  CUtensorMap tm_qc = tm;
+  if (args.q_col != nullptr && (args.flags & kFlagFp8) == 0) {
+    cuuint64_t qdims[2] = {static_cast<cuuint64_t>(args.rows / 2), static_cast<cuuint64_t>(args.cols)};
+    cuuint64_t qstrides[1] = {static_cast<cuuint64_t>(args.rows / 2)};
+    cuuint32_t qbox[2] = {64, 128};
+    if (fn(&tm_qc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, args.q_col, qdims, qstrides, qbox, estrides,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -522,11 +572,11 @@ cudaError_t launch_cast(const CastArgs& args, cudaStream_t stream) {
   const bool row = args.q_row != nullptr, col = args.q_col != nullptr;
   if (args.flags & kFlagFp8) {
     if (row || !col) return cudaErrorInvalidValue;  // MXFP8: column output only
-    return launch_had<false, true, true>(tm, args, ct, rt, ns, dev, stream);
+    return launch_had<false, true, true>(tm, tm_qc, args, ct, rt, ns, dev, stream);
   }
-  if (row && col) return launch_had<true, true, false>(tm, args, ct, rt, ns, dev, stream);
-  if (row) return launch_had<true, false, false>(tm, args, ct, rt, ns, dev, stream);
-  if (col) return launch_had<false, true, false>(tm, args, ct, rt, ns, dev, stream);
+  if (row && col) return launch_had<true, true, false>(tm, tm_qc, args, ct, rt, ns, dev, stream);
+  if (row) return launch_had<true, false, false>(tm, tm_qc, args, ct, rt, ns, dev, stream);
+  if (col) return launch_had<false, true, false>(tm, tm_qc, args, ct, rt, ns, dev, stream);
   return cudaSuccess;
 }
 
