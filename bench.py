@@ -9,10 +9,11 @@ quotes):
                        (column copy with the Hadamard);
   three MXFP4 GEMMs -- fwd Y = X W^T, dgrad dX = dY W, wgrad dW = dY^T X.
 `value` is the step's GEMM TFLOP/s (3 x 2MNK per step over the step time,
-casts included) with inputs resident in HBM.  A step is four launches: the
-three casts side by side on three streams, then the three GEMMs in one
-gemm_fp4_grouped launch (--serial-step puts the casts on one stream,
---separate-gemms times six launches with three gemm_fp4 instead); `e2e` repeats it through the same
+casts included) with inputs resident in HBM.  A step is two launches: the
+three casts in one mxfp4_cast_dual_grouped launch, then the three GEMMs in one
+gemm_fp4_grouped launch (--separate-casts times four launches, the three casts
+side by side on three streams or, with --serial-step, on one; --separate-gemms
+six, with three gemm_fp4); `e2e` repeats it through the same
 C-ABI calls with host buffers (pinned H2D of X, W, dY and D2H of Y, dX, dW of
 every step inside the timed region, double-buffered so that one step's uploads
 and downloads overlap its neighbours' compute).  `--impl reference` times the
@@ -201,6 +202,13 @@ class Step:
             if events is not None:
                 events[i][1].record(stream)
 
+    def casts_grouped(self, stream, xs=None):
+        """The dual casts of X and dY (column Hadamard) and W in one
+        mxfp4_cast_dual_grouped launch."""
+        x, w, dy = xs if xs is not None else (self.x, self.w, self.dy)
+        return self.m.mxfp4_cast_dual_grouped([(x, False, True, self.qx), (w, False, False, self.qw),
+                                               (dy, False, True, self.qdy)], stream=stream)
+
     def gemms_grouped(self, stream, outs=None):
         """fwd, dgrad and wgrad in one gemm_fp4_grouped launch."""
         m = self.m
@@ -210,11 +218,14 @@ class Step:
             (self.qdy[0], self.qdy[1], self.qw[2], self.qw[3], M, K, N, dx),
             (self.qdy[2], self.qdy[3], self.qx[2], self.qx[3], N, K, M, dw)], stream=stream)
 
-    def run_grouped(self, stream, side=None):
-        """The step as four launches: the casts of X, W and dY (side by side on
-        three streams when `side` is given), then one grouped launch of the
-        three GEMMs once all three casts are done."""
-        if side is None:
+    def run_grouped(self, stream, side=None, casts_grouped=True):
+        """The step as two launches: the casts of X, W and dY in one grouped
+        launch, then the three GEMMs in one.  With casts_grouped=False, four:
+        the three casts (side by side on three streams when `side` is given),
+        then the grouped GEMM launch once all three are done."""
+        if casts_grouped:
+            self.casts_grouped(stream)
+        elif side is None:
             for _, f in self.launches(stream)[:3]:
                 f()
         else:
@@ -275,13 +286,13 @@ class Step:
         m = self.m
         x, w, dy = xs
         y, dx, dw = outs
+        if grouped:  # one grouped cast launch and one grouped GEMM launch
+            return [lambda: self.casts_grouped(stream, xs), lambda: self.gemms_grouped(stream, outs)]
         casts = [
             lambda: m.mxfp4_cast_dual(x, hadamard_col=True, out=self.qx, stream=stream),
             lambda: m.mxfp4_cast_dual(w, out=self.qw, stream=stream),
             lambda: m.mxfp4_cast_dual(dy, hadamard_col=True, out=self.qdy, stream=stream),
         ]
-        if grouped:
-            return casts + [lambda: self.gemms_grouped(stream, outs)]
         return casts + [
             lambda: m.gemm_fp4(self.qx[0], self.qx[1], self.qw[0], self.qw[1], M, N, K, c=y, stream=stream),
             lambda: m.gemm_fp4(self.qdy[0], self.qdy[1], self.qw[2], self.qw[3], M, K, N, c=dx, stream=stream),
@@ -835,7 +846,9 @@ def main():
     ap.add_argument("--serial-step", action="store_true",
                     help="capture the step's launches on one stream instead of three")
     ap.add_argument("--separate-gemms", action="store_true",
-                    help="time the step as six launches (three gemm_fp4) instead of one grouped GEMM launch")
+                    help="time the step as six launches (three casts, three gemm_fp4)")
+    ap.add_argument("--separate-casts", action="store_true",
+                    help="time the step as four launches (three casts, one grouped GEMM launch) instead of two")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
         log("warmup raised to 3 (minimum)")
@@ -863,7 +876,7 @@ def main():
             else:
                 step.run_concurrent(stream, side)
         else:
-            step.run_grouped(stream, None if args.serial_step else side)
+            step.run_grouped(stream, None if args.serial_step else side, casts_grouped=not args.separate_casts)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -878,11 +891,12 @@ def main():
         return 3
 
     # --------------------------------------------------------------- timed region (HBM-resident inputs)
-    # One step (4 launches through the C ABI: three casts and one grouped GEMM;
-    # 6 with --separate-gemms) is captured once as a CUDA graph and replayed K
-    # times, so the host never starves the GPU between launches.
+    # One step (2 launches through the C ABI: one grouped cast launch and one
+    # grouped GEMM launch; 4 with --separate-casts, 6 with --separate-gemms) is
+    # captured once as a CUDA graph and replayed K times, so the host never
+    # starves the GPU between launches.
     n_launch = len(step.launches(stream))
-    n_launch_step = n_launch if args.separate_gemms else 4
+    n_launch_step = n_launch if args.separate_gemms else (4 if args.separate_casts else 2)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         timed_step()
@@ -956,6 +970,16 @@ def main():
             cev[i][1].record(stream)
     stream.synchronize()
     cast_chain_t = [a.elapsed_time(b) / 1e3 for a, b in cev]
+    # the three casts in one grouped launch, the step's form
+    qev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_prof)]
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int((0.005 + 2.0 * n_prof * host_per_step) * 2.2e9))
+        for i in range(n_prof):
+            qev[i][0].record(stream)
+            step.casts_grouped(stream)
+            qev[i][1].record(stream)
+    stream.synchronize()
+    cast_grouped_t = [a.elapsed_time(b) / 1e3 for a, b in qev]
     kinds = [k for k, _ in step.launches(stream)]
     per = [[evs[i][j][0].elapsed_time(evs[i][j][1]) / 1e3 for j in range(n_launch)] for i in range(n_prof)]
     gemm_t = [sum(p[j] for j in range(n_launch) if kinds[j] == "gemm") for p in per]
@@ -990,8 +1014,11 @@ def main():
         "cast_frac_of_8tbs": cast_gbs / 8000.0,
         "casts_back_to_back_us": statistics.mean(cast_chain_t) * 1e6,
         "casts_back_to_back_frac_of_hbm_measured": cast_bytes / statistics.mean(cast_chain_t) / 1e9 / peaks["hbm"],
+        "casts_grouped_us": statistics.mean(cast_grouped_t) * 1e6,
+        "casts_grouped_frac_of_hbm_measured": cast_bytes / statistics.mean(cast_grouped_t) / 1e9 / peaks["hbm"],
         "casts_what": "cast_us: each cast between its own event pair (no overlap with its neighbours); "
-                      "casts_back_to_back: the three in a row with events only around them",
+                      "casts_back_to_back: the three in a row with events only around them; "
+                      "casts_grouped: the three in one mxfp4_cast_dual_grouped launch (the step's form)",
     }
 
     # --------------------------------------------------------------- e2e leg (host buffers)
@@ -1067,13 +1094,17 @@ def main():
             "e2e": e2e,
             "gpu_launches": n_launch_step * args.steps,
             "timing": {"timed_region": ("CUDA-graph replay of the captured step, K times, CUDA events on the launch stream; "
-                                        + ("six launches (three gemm_fp4)" if args.separate_gemms else
-                                           "four launches (three casts, one gemm_fp4_grouped of fwd, dgrad and wgrad)")
-                                        + ("" if args.serial_step else
-                                           ", the casts side by side on three streams")),
-                       "per_kernel": f"{n_prof} eager steps of six launches, {n_prof} eager grouped GEMM launches and "
-                                     f"{n_prof} runs of the three casts back to back, each enqueued behind a GPU sleep, "
-                                     "an event pair per launch (per run for the casts back to back)"},
+                                        + ("six launches (three casts, three gemm_fp4)" if args.separate_gemms else
+                                           "four launches (three casts, one gemm_fp4_grouped of fwd, dgrad and wgrad)"
+                                           if args.separate_casts else
+                                           "two launches (one mxfp4_cast_dual_grouped of X, W and dY, one "
+                                           "gemm_fp4_grouped of fwd, dgrad and wgrad)")
+                                        + ("" if args.serial_step or not (args.separate_gemms or args.separate_casts)
+                                           else ", the casts side by side on three streams")),
+                       "per_kernel": f"{n_prof} eager steps of six launches, {n_prof} eager grouped GEMM launches, "
+                                     f"{n_prof} runs of the three casts back to back and {n_prof} grouped cast launches, "
+                                     "each enqueued behind a GPU sleep, an event pair per launch (per run for the "
+                                     "casts back to back)"},
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)

@@ -124,6 +124,37 @@ mxfp4_status mxfp4_cast_dual(const uint16_t* x, int64_t rows, int64_t cols, int6
                              uint32_t flags, void* stream);
 
 /*
+ * mxfp4_cast_dual_grouped -- up to MXFP4_GROUP_MAX independent mxfp4_cast_dual
+ * calls in one launch.  A training step casts X, W and dY before its GEMMs
+ * (the "FP4 GEMM (training)" row: every operand goes through the cast); one
+ * persistent launch over all their tiles (numbered cast after cast) fills
+ * and drains the pipeline once instead of once per cast.  The pages describe
+ * no grouped call: this is a scheduling form of mxfp4_cast_dual with the same
+ * results, every byte equal to the mxfp4_cast_dual call with the same
+ * arguments.
+ *   casts : host array of `count` descriptors, read during the call only;
+ *           each field means what the mxfp4_cast_dual argument of the same
+ *           name means (each its own shape and flags)
+ *   count : 1 .. MXFP4_GROUP_MAX
+ * Each descriptor is checked as mxfp4_cast_dual checks its arguments, in
+ * that order.  The first failing descriptor's status is returned and nothing
+ * is launched.  Descriptors with rows == 0 or cols == 0 are skipped.  Every
+ * cast's memory must be on one device (MXFP4_ERR_INVALID_ARG otherwise).
+ * The casts run concurrently: no output may overlap another descriptor's
+ * input or outputs.
+ */
+typedef struct mxfp4_cast_desc {
+  const uint16_t* x;
+  int64_t rows, cols, ldx;
+  uint8_t* q_row;
+  uint8_t* sf_row;
+  uint8_t* q_col;
+  uint8_t* sf_col;
+  uint32_t flags;
+} mxfp4_cast_desc;
+mxfp4_status mxfp4_cast_dual_grouped(const mxfp4_cast_desc* casts, int count, void* stream);
+
+/*
  * gemm_fp4 -- C[M,N] = A[M,K] . B[N,K]^T on MXFP4 operands, bf16 output
  * (gemm_fp4 of the "FP4 GEMM (low-level)" row).
  *   a, a_sf : codes [M, K/2], scales (tile layout, M rows, K/32 blocks)

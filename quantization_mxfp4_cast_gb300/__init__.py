@@ -37,6 +37,12 @@ class GemmDesc(ctypes.Structure):
                 ("b_sf", ctypes.c_void_p), ("c", ctypes.c_void_p), ("M", ctypes.c_int64),
                 ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("ldc", ctypes.c_int64)]
 
+class CastDesc(ctypes.Structure):
+    """mxfp4_cast_desc: one cast of a mxfp4_cast_dual_grouped call."""
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("ldx", ctypes.c_int64), ("q_row", ctypes.c_void_p), ("sf_row", ctypes.c_void_p),
+                ("q_col", ctypes.c_void_p), ("sf_col", ctypes.c_void_p), ("flags", ctypes.c_uint32)]
+
 # Every extern "C" symbol declared in include/mxfp4.h.
 ABI_SYMBOLS = (
     "mxfp4_abi_version", "mxfp4_status_string", "mxfp4_codes_bytes", "mxfp4_scales_bytes",
@@ -44,7 +50,7 @@ ABI_SYMBOLS = (
     "gemm_fp4_bf16_fwd", "gemm_fp4_bf16_dgrad", "gemm_fp4_bf16_wgrad", "mxfp4_device_status",
     "gemm_fp4_bf16_fwd_noalloc", "mxfp4_last_cuda_error", "mxfp4_cuda_error_string",
     "mxfp8_cast_cols", "gemm_mxfp8", "gemm_fp8_bf16_wgrad", "gemm_fp4_cast_out",
-    "mxfp4_selftest_wait_timeout", "gemm_fp4_grouped",
+    "mxfp4_selftest_wait_timeout", "gemm_fp4_grouped", "mxfp4_cast_dual_grouped",
 )
 
 _lib = None
@@ -95,6 +101,7 @@ def lib() -> ctypes.CDLL:
                 "gemm_fp4_cast_out": (I, [P, P, P, P, P, I64, I64, I64, I64, P, P, P, P, U32, P]),
                 "mxfp4_selftest_wait_timeout": (I, [P, P, P, P, P, I64, I64, I64, I64, ctypes.c_uint64, P]),
                 "gemm_fp4_grouped": (I, [ctypes.POINTER(GemmDesc), I, P]),
+                "mxfp4_cast_dual_grouped": (I, [ctypes.POINTER(CastDesc), I, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -183,6 +190,33 @@ def mxfp4_cast_dual(x, hadamard_row: bool = False, hadamard_col: bool = False,
     _check(lib().mxfp4_cast_dual(_ptr(x), R, C, x.stride(0), _ptr(q_row), _ptr(sf_row), _ptr(q_col),
                                  _ptr(sf_col), flags, _stream(stream)), "mxfp4_cast_dual")
     return q_row, sf_row, q_col, sf_col
+
+
+def mxfp4_cast_dual_grouped(casts, stream=None):
+    """Up to MXFP4_GROUP_MAX dual casts in one launch.  `casts` holds tuples
+    (x, hadamard_row, hadamard_col[, out]); returns, per cast, the
+    (q_row, sf_row, q_col, sf_col) that mxfp4_cast_dual would, byte for byte."""
+    descs = (CastDesc * max(len(casts), 1))()
+    outs = []
+    for i, item in enumerate(casts):
+        x, had_row, had_col = item[:3]
+        out = item[3] if len(item) > 3 else None
+        _bf16_2d(x, "x")
+        _need_cuda(x)
+        R, C = x.shape
+        if out is None:
+            dev = x.device
+            out = (torch.empty(R, C // 2, dtype=torch.uint8, device=dev),
+                   torch.empty(scales_bytes(R, C), dtype=torch.uint8, device=dev),
+                   torch.empty(C, R // 2, dtype=torch.uint8, device=dev),
+                   torch.empty(scales_bytes(C, R), dtype=torch.uint8, device=dev))
+        q_row, sf_row, q_col, sf_col = out
+        flags = (MXFP4_HADAMARD_ROW if had_row else 0) | (MXFP4_HADAMARD_COL if had_col else 0)
+        descs[i] = CastDesc(_ptr(x), R, C, x.stride(0), _ptr(q_row), _ptr(sf_row), _ptr(q_col), _ptr(sf_col),
+                            flags)
+        outs.append(tuple(out))
+    _check(lib().mxfp4_cast_dual_grouped(descs, len(casts), _stream(stream)), "mxfp4_cast_dual_grouped")
+    return outs
 
 
 # ----------------------------------------------------------------------------- GEMM

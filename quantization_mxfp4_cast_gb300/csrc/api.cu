@@ -239,21 +239,58 @@ mxfp4_status mxfp4_cast(const uint16_t* x, int64_t rows, int64_t cols, int64_t l
   return from_cuda(mxfp4::launch_cast(a, static_cast<cudaStream_t>(stream)));
 }
 
-mxfp4_status mxfp4_cast_dual(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
-                             uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col,
-                             uint32_t flags, void* stream) {
+// The checks of mxfp4_cast_dual, in its order; binds the device of x.
+// `*empty` is set when there is nothing to cast.
+static mxfp4_status check_cast_dual(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
+                                    const uint8_t* q_row, const uint8_t* sf_row, const uint8_t* q_col,
+                                    const uint8_t* sf_col, uint32_t flags, bool* empty) {
+  *empty = false;
   if (flags & ~(MXFP4_HADAMARD_ROW | MXFP4_HADAMARD_COL | MXFP4_SCALE_LINEAR))
     return MXFP4_ERR_INVALID_ARG;
   MXFP4_TRY(check_bf16_in(x, rows, cols, ldx));
   if (rows % 32 != 0) return MXFP4_ERR_INVALID_ARG;
-  if (rows == 0 || cols == 0) return MXFP4_OK;
+  if (rows == 0 || cols == 0) {
+    *empty = true;
+    return MXFP4_OK;
+  }
   MXFP4_TRY(check_out(q_row));
   MXFP4_TRY(check_out(sf_row));
   MXFP4_TRY(check_out(q_col));
   MXFP4_TRY(check_out(sf_col));
-  MXFP4_TRY(check_device(x));
+  return check_device(x);
+}
+
+mxfp4_status mxfp4_cast_dual(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
+                             uint8_t* q_row, uint8_t* sf_row, uint8_t* q_col, uint8_t* sf_col,
+                             uint32_t flags, void* stream) {
+  bool empty = false;
+  MXFP4_TRY(check_cast_dual(x, rows, cols, ldx, q_row, sf_row, q_col, sf_col, flags, &empty));
+  if (empty) return MXFP4_OK;
   CastArgs a{x, rows, cols, ldx, q_row, sf_row, q_col, sf_col, flags};
   return from_cuda(mxfp4::launch_cast(a, static_cast<cudaStream_t>(stream)));
+}
+
+mxfp4_status mxfp4_cast_dual_grouped(const mxfp4_cast_desc* casts, int count, void* stream) {
+  if (casts == nullptr || count < 1 || count > MXFP4_GROUP_MAX) return MXFP4_ERR_INVALID_ARG;
+  CastArgs list[MXFP4_GROUP_MAX];
+  int n = 0, dev = -1;
+  for (int i = 0; i < count; ++i) {
+    const mxfp4_cast_desc& d = casts[i];
+    bool empty = false;
+    MXFP4_TRY(check_cast_dual(d.x, d.rows, d.cols, d.ldx, d.q_row, d.sf_row, d.q_col, d.sf_col, d.flags,
+                              &empty));
+    if (empty) continue;
+    int cur = 0;
+    cudaError_t e = cudaGetDevice(&cur);  // the device check_cast_dual bound
+    if (e != cudaSuccess) return from_cuda(e);
+    if (dev >= 0 && cur != dev) return MXFP4_ERR_INVALID_ARG;  // one launch, one device
+    dev = cur;
+    list[n++] = CastArgs{d.x, d.rows, d.cols, d.ldx, d.q_row, d.sf_row, d.q_col, d.sf_col, d.flags};
+  }
+  if (n == 0) return MXFP4_OK;
+  cudaError_t e = mxfp4::launch_cast_grouped(list, n, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidValue) return MXFP4_ERR_INVALID_ARG;
+  return from_cuda(e);
 }
 
 mxfp4_status gemm_fp4(const uint8_t* a, const uint8_t* a_sf, const uint8_t* b, const uint8_t* b_sf,

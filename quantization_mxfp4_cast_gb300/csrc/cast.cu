@@ -111,6 +111,31 @@ __device__ __forceinline__ void block_codes(V v, uint32_t* out) {
   }
 }
 
+// Up to kMaxCastGroup casts in one launch: their tiles are numbered one cast
+// after another, and every slab carries its cast's index.
+constexpr int kMaxCastGroup = 4;
+struct CastMaps {
+  CUtensorMap x[kMaxCastGroup];   // bf16 input, 32 x 64 boxes
+  CUtensorMap qc[kMaxCastGroup];  // MXFP4 column codes, 128 x 64-byte boxes
+};
+struct CastGroup {
+  CastArgs args;
+  int col_tiles, row_tiles128;
+  int tile_end;  // tiles of this cast and the ones before it
+};
+struct CastGroups {
+  CastGroup g[kMaxCastGroup];
+  int count, num_tiles;
+};
+
+// The cast of tile t (0 <= t < num_tiles) and t's index within that cast.
+__device__ __forceinline__ int cast_of_tile(const CastGroups& p, int t, int& lt) {
+  int g = 0;
+  while (g + 1 < p.count && t >= p.g[g].tile_end) ++g;
+  lt = g == 0 ? t : t - p.g[g - 1].tile_end;
+  return g;
+}
+
 // Byte of (row r, block b) inside a 512-byte scale tile of 128 rows x 4 blocks.
 __device__ __forceinline__ int sf_in_tile(int r, int b) { return (r & 31) * 16 + ((r >> 5) & 3) * 4 + b; }
 
@@ -147,11 +172,9 @@ __device__ __forceinline__ bool wait_word(const uint32_t* p, uint32_t want, vola
 // slabs of the last, partial round of tiles are dealt out one by one over all
 // CTAs (tail slab u goes to CTA u mod G), so that every CTA's work is within
 // one slab of every other's; a tail slab writes its scale bytes directly.
-template <bool kRow, bool kCol, bool kFp8, bool kHadRow, bool kHadCol>
+template <bool kRow, bool kCol, bool kFp8, int kHadRowMode, int kHadColMode>
 __global__ void __launch_bounds__(kThreads, 1)
-    cast_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmQc,
-                const CastArgs args, int col_tiles,
-                int row_tiles128, int num_tiles, int* status) {
+    cast_kernel(const __grid_constant__ CastMaps maps, const __grid_constant__ CastGroups p, int* status) {
   static_assert(!(kFp8 && kRow), "MXFP8 is produced column-wise only");
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment: the swizzle pattern follows address bits 7..9.
@@ -173,8 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t rows = args.rows, cols = args.cols;
-  const bool linear = (args.flags & kFlagScaleLinear) != 0;
+  const int num_tiles = p.num_tiles;
   // local slabs of this CTA: four per whole tile, then its tail slabs
   const int grid = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
   const int full_rounds = num_tiles / grid;
@@ -199,7 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 0;
     }
   }
-  if (threadIdx.x == 32 * kConsumerWarps) tma_prefetch_desc(&tmX);
+  if (threadIdx.x == 32 * kConsumerWarps)
+    for (int g = 0; g < p.count; ++g) tma_prefetch_desc(&maps.x[g]);
   __syncthreads();
   // x may be the output of the previous kernel in the stream, and the outputs
   // may still be read by it: nothing below touches global memory before it ends.
@@ -210,32 +233,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int issued = 0;
-      // tile coordinates advance by the grid size each step (no divisions in the loop)
-      int tx = static_cast<int>(blockIdx.x) % col_tiles, ty = static_cast<int>(blockIdx.x) / col_tiles;
-      const int step_x = static_cast<int>(gridDim.x) % col_tiles, step_y = static_cast<int>(gridDim.x) / col_tiles;
       int slot = 0;
       uint32_t empty_parity = 1;  // from the second pass on: parity of the slot's previous release
       bool ok = true;
+      int g = 0, tx = 0, ty = 0;  // the current whole tile: its cast and coordinates
       for (int i = 0; ok && i < n_local; ++i) {
         const int j = i & 3;
         int rb, ct;
         uint32_t tail_bit = 0;
         if (i < n_whole) {
+          if (j == 0) {  // a new whole tile (32-bit divisions, once per four slabs)
+            int lt;
+            g = cast_of_tile(p, cta + (i >> 2) * grid, lt);
+            ty = lt / p.g[g].col_tiles;
+            tx = lt - ty * p.g[g].col_tiles;
+          }
           rb = 4 * ty + j;
           ct = tx;
-          if (j == 3) {
-            tx += step_x;
-            ty += step_y;
-            if (tx >= col_tiles) {
-              tx -= col_tiles;
-              ++ty;
-            }
-          }
         } else {  // tail slab u of the partial round (a handful per CTA)
           const int u = cta + (i - n_whole) * grid;
-          const int tile = full_rounds * grid + u / 4;
-          rb = 4 * (tile / col_tiles) + (u & 3);
-          ct = tile % col_tiles;
+          int lt;
+          g = cast_of_tile(p, full_rounds * grid + u / 4, lt);
+          rb = 4 * (lt / p.g[g].col_tiles) + (u & 3);
+          ct = lt % p.g[g].col_tiles;
           tail_bit = 0x80000000u;
         }
         // the slot's previous slab (i - kStages) has been quantized
@@ -244,12 +264,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         slot_rb[slot] = static_cast<uint32_t>(rb) | tail_bit;
-        slot_ct[slot] = static_cast<uint32_t>(ct);
+        slot_ct[slot] = static_cast<uint32_t>(ct) | (static_cast<uint32_t>(g) << 28);
         st_release_shared(&seq[slot], static_cast<uint32_t>(i));  // publishes the coordinates too
         uint8_t* dst = ring + slot * kSlabBytes;
         mbar_arrive_expect_tx(&full[slot], kSlabBytes);
-        tma_load_2d(dst, &tmX, &full[slot], ct * kSlabCols, rb * kSlabRows);
-        tma_load_2d(dst + kHalfBytes, &tmX, &full[slot], ct * kSlabCols + kSlabCols / 2, rb * kSlabRows);
+        tma_load_2d(dst, &maps.x[g], &full[slot], ct * kSlabCols, rb * kSlabRows);
+        tma_load_2d(dst + kHalfBytes, &maps.x[g], &full[slot], ct * kSlabCols + kSlabCols / 2, rb * kSlabRows);
         issued = i + 1;
         if (++slot == kStages) {
           slot = 0;
@@ -278,7 +298,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!wait_word(&seq[slot], static_cast<uint32_t>(i), abort_flag, status)) break;
     const uint32_t rbw = slot_rb[slot];  // 32-row block (published with seq), bit 31: tail slab
     const int rb = static_cast<int>(rbw & 0x7FFFFFFFu);
-    const int ct = static_cast<int>(slot_ct[slot]);
+    const uint32_t ctw = slot_ct[slot];  // 128-column tile, bits 28-29: the cast
+    const int ct = static_cast<int>(ctw & 0x0FFFFFFFu);
+    const int g = static_cast<int>(ctw >> 28);
+    const CastArgs& args = p.g[g].args;
+    const int col_tiles = p.g[g].col_tiles, row_tiles128 = p.g[g].row_tiles128;
+    const int64_t rows = args.rows, cols = args.cols;
+    const bool linear = (args.flags & kFlagScaleLinear) != 0;
+    const bool had_row = kHadRowMode == 2 ? (args.flags & kFlagHadamardRow) != 0 : kHadRowMode == 1;
+    const bool had_col = kHadColMode == 2 ? (args.flags & kFlagHadamardCol) != 0 : kHadColMode == 1;
     // scale bytes: staged per whole tile, or straight to the tile layout (tail slab)
     const bool staged = !linear && (rbw >> 31) == 0;
     const int sfb = (i >> 2) % kSfBufs;  // the whole tile's staging buffer
@@ -318,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint32_t c[4];
         BlockScale sc;
-        if constexpr (!kHadRow) {
+        if (!had_row) {
           sc = quantize_bf16_block(v, c);
         } else {
           float y[32];
@@ -357,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           w[k] = *reinterpret_cast<const uint32_t*>(colp + k * 128 + ((ch ^ (k & 7)) << 4));
         BlockScale sa, sb;
         uint32_t ca[kWords], cb[kWords];  // codes of columns 2p and 2p + 1
-        if constexpr (!kHadCol) {
+        if (!had_col) {
           const uint32_t m = tree_absmax_bf16x2<32>(w) & 0x7FFF7FFFu;
           sa = block_scale<kEmax>(m << 16);
           sb = block_scale<kEmax>(m & 0xFFFF0000u);
@@ -461,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (cq_staged && lane == 0) {
           // the tile's column codes: 128 columns x 64 bytes (rows past the end
           // and columns past cols are clipped by the store)
-          tma_store_2d(&tmQc, cq_stage + cqb * kCqBytes, static_cast<int32_t>(tile_y * 64),
+          tma_store_2d(&maps.qc[g], cq_stage + cqb * kCqBytes, static_cast<int32_t>(tile_y * 64),
                        static_cast<int32_t>(tile_x * 128));
           bulk_commit_group();
           bulk_wait_group_read0();  // the buffer has been read
@@ -478,10 +506,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (lane == 0) bulk_wait_group0();  // this warp's column-code stores are complete
 }
 
-template <bool kRow, bool kCol, bool kFp8, bool kHadRow, bool kHadCol>
-cudaError_t launch_cast_t(const CUtensorMap& tm, const CUtensorMap& tm_qc, const CastArgs& args, int col_tiles,
-                          int row_tiles128, int num_tiles, int dev, cudaStream_t stream) {
-  auto kernel = cast_kernel<kRow, kCol, kFp8, kHadRow, kHadCol>;
+template <bool kRow, bool kCol, bool kFp8, int kHadRowMode, int kHadColMode>
+cudaError_t launch_cast_t(const CastMaps& maps, const CastGroups& groups, int dev, cudaStream_t stream) {
+  auto kernel = cast_kernel<kRow, kCol, kFp8, kHadRowMode, kHadColMode>;
   static std::atomic<int> ctas[64];  // resident CTAs on the whole GPU, per device
   int grid = (dev >= 0 && dev < 64) ? ctas[dev].load(std::memory_order_relaxed) : 0;
   if (grid == 0) {
@@ -500,7 +527,7 @@ cudaError_t launch_cast_t(const CUtensorMap& tm, const CUtensorMap& tm_qc, const
   // cudaLaunchKernelEx reports this launch's own error; the thread's last
   // error may hold a stale, unrelated one (e.g. a not-ready query result).
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(4 * static_cast<int64_t>(num_tiles), grid)), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(4 * static_cast<int64_t>(groups.num_tiles), grid)), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kCastSmemBytes;
   cfg.stream = stream;
@@ -509,75 +536,117 @@ cudaError_t launch_cast_t(const CUtensorMap& tm, const CUtensorMap& tm_qc, const
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, status);
+  return cudaLaunchKernelEx(&cfg, kernel, maps, groups, status);
 }
 
+// Hadamard flags of a launch: off (0) or on (1) for every cast in it, or per
+// cast at run time (2) where they differ.
 template <bool kRow, bool kCol, bool kFp8>
-cudaError_t launch_had(const CUtensorMap& tm, const CUtensorMap& tm_qc, const CastArgs& args, int col_tiles,
-                       int row_tiles128, int num_tiles, int dev, cudaStream_t stream) {
-  const bool hr = kRow && (args.flags & kFlagHadamardRow) != 0;
-  const bool hc = kCol && (args.flags & kFlagHadamardCol) != 0;
+cudaError_t launch_had(const CastMaps& maps, const CastGroups& groups, int dev, cudaStream_t stream) {
+  auto mode = [&](uint32_t flag, bool applies) {
+    if (!applies) return 0;
+    int on = 0;
+    for (int g = 0; g < groups.count; ++g) on += (groups.g[g].args.flags & flag) != 0;
+    return on == 0 ? 0 : (on == groups.count ? 1 : 2);
+  };
+  const int hr = mode(kFlagHadamardRow, kRow), hc = mode(kFlagHadamardCol, kCol);
   if constexpr (kRow && kCol) {
-    if (hr && hc) return launch_cast_t<true, true, kFp8, true, true>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
-    if (hr) return launch_cast_t<true, true, kFp8, true, false>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
-    if (hc) return launch_cast_t<true, true, kFp8, false, true>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
-    return launch_cast_t<true, true, kFp8, false, false>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    if (hr == 2 || hc == 2) return launch_cast_t<true, true, kFp8, 2, 2>(maps, groups, dev, stream);
+    if (hr && hc) return launch_cast_t<true, true, kFp8, 1, 1>(maps, groups, dev, stream);
+    if (hr) return launch_cast_t<true, true, kFp8, 1, 0>(maps, groups, dev, stream);
+    if (hc) return launch_cast_t<true, true, kFp8, 0, 1>(maps, groups, dev, stream);
+    return launch_cast_t<true, true, kFp8, 0, 0>(maps, groups, dev, stream);
   } else if constexpr (kRow) {
-    if (hr) return launch_cast_t<true, false, kFp8, true, false>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
-    return launch_cast_t<true, false, kFp8, false, false>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    if (hr == 2) return launch_cast_t<true, false, kFp8, 2, 0>(maps, groups, dev, stream);
+    if (hr) return launch_cast_t<true, false, kFp8, 1, 0>(maps, groups, dev, stream);
+    return launch_cast_t<true, false, kFp8, 0, 0>(maps, groups, dev, stream);
   } else {
-    if (hc) return launch_cast_t<false, true, kFp8, false, true>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
-    return launch_cast_t<false, true, kFp8, false, false>(tm, tm_qc, args, col_tiles, row_tiles128, num_tiles, dev, stream);
+    if (hc == 2) return launch_cast_t<false, true, kFp8, 0, 2>(maps, groups, dev, stream);
+    if (hc) return launch_cast_t<false, true, kFp8, 0, 1>(maps, groups, dev, stream);
+    return launch_cast_t<false, true, kFp8, 0, 0>(maps, groups, dev, stream);
   }
 }
 
-}  // namespace
-
-cudaError_t launch_cast(const CastArgs& args, cudaStream_t stream) {
-  if (args.rows == 0 || args.cols == 0) return cudaSuccess;
-  EncodeTiledFn fn = encode_tiled_fn();
-  if (!fn) return cudaErrorNotSupported;
-  CUtensorMap tm;
+// Tensor maps and tile counts of one cast; false if a map cannot be encoded
+// or the tile counts leave the 32-bit range.
+bool prepare_cast(const CastArgs& args, EncodeTiledFn fn, CUtensorMap* tm, CUtensorMap* tm_qc, CastGroup* grp) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(args.cols), static_cast<cuuint64_t>(args.rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(args.ldx) * 2};
   cuuint32_t box[2] = {kSlabCols / 2, kSlabRows};  // 64 columns (128 bytes) x 32 rows
   cuuint32_t estrides[2] = {1, 1};
-  if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(args.x), dims, strides, box,
+  if (fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(args.x), dims, strides, box,
          estrides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+    return false;
   // column codes [cols, rows / 2] (MXFP4), stored a tile (128 columns x 64
   // bytes) at a time from a 64-byte-swizzled staging buffer
-  CUtensorMap tm_qc = tm;
+  *tm_qc = *tm;
   if (args.q_col != nullptr && (args.flags & kFlagFp8) == 0) {
     cuuint64_t qdims[2] = {static_cast<cuuint64_t>(args.rows / 2), static_cast<cuuint64_t>(args.cols)};
     cuuint64_t qstrides[1] = {static_cast<cuuint64_t>(args.rows / 2)};
     cuuint32_t qbox[2] = {64, 128};
-    if (fn(&tm_qc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, args.q_col, qdims, qstrides, qbox, estrides,
+    if (fn(tm_qc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, args.q_col, qdims, qstrides, qbox, estrides,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+      return false;
   }
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
   const int64_t col_tiles = (args.cols + kSlabCols - 1) / kSlabCols;
   const int64_t row_tiles128 = (args.rows + 127) / 128;
   // whole 128 x 128 tiles: the slabs past the last row only write the zero
   // scales of the tile padding
   const int64_t num_tiles = row_tiles128 * col_tiles;
-  if (4 * num_tiles > (int64_t(1) << 31) - 1 || row_tiles128 * 128 > (int64_t(1) << 31) - 1)
-    return cudaErrorInvalidValue;
-  const int ns = static_cast<int>(num_tiles), ct = static_cast<int>(col_tiles), rt = static_cast<int>(row_tiles128);
-  const bool row = args.q_row != nullptr, col = args.q_col != nullptr;
-  if (args.flags & kFlagFp8) {
-    if (row || !col) return cudaErrorInvalidValue;  // MXFP8: column output only
-    return launch_had<false, true, true>(tm, tm_qc, args, ct, rt, ns, dev, stream);
+  if (4 * num_tiles > (int64_t(1) << 31) - 1 || row_tiles128 * 128 > (int64_t(1) << 31) - 1 ||
+      col_tiles >= (int64_t(1) << 28))
+    return false;
+  grp->args = args;
+  grp->col_tiles = static_cast<int>(col_tiles);
+  grp->row_tiles128 = static_cast<int>(row_tiles128);
+  grp->tile_end = static_cast<int>(num_tiles);  // made cumulative by the caller
+  return true;
+}
+
+}  // namespace
+
+cudaError_t launch_cast_grouped(const CastArgs* list, int count, cudaStream_t stream) {
+  if (count < 1 || count > kMaxCastGroup) return cudaErrorInvalidValue;
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return cudaErrorNotSupported;
+  CastMaps maps = {};
+  CastGroups groups = {};
+  int64_t tiles = 0;
+  bool row = false, col = false, fp8 = false, first = true;
+  for (int i = 0; i < count; ++i) {
+    const CastArgs& args = list[i];
+    if (args.rows == 0 || args.cols == 0) continue;
+    const bool r = args.q_row != nullptr, c = args.q_col != nullptr, f = (args.flags & kFlagFp8) != 0;
+    if (!r && !c) continue;
+    // one kind of cast per launch: the same outputs and element format
+    if (!first && (r != row || c != col || f != fp8)) return cudaErrorInvalidValue;
+    row = r, col = c, fp8 = f, first = false;
+    CastGroup& grp = groups.g[groups.count];
+    if (!prepare_cast(args, fn, &maps.x[groups.count], &maps.qc[groups.count], &grp))
+      return cudaErrorInvalidValue;
+    tiles += grp.tile_end;
+    if (4 * tiles > (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
+    grp.tile_end = static_cast<int>(tiles);
+    ++groups.count;
   }
-  if (row && col) return launch_had<true, true, false>(tm, tm_qc, args, ct, rt, ns, dev, stream);
-  if (row) return launch_had<true, false, false>(tm, tm_qc, args, ct, rt, ns, dev, stream);
-  if (col) return launch_had<false, true, false>(tm, tm_qc, args, ct, rt, ns, dev, stream);
-  return cudaSuccess;
+  if (groups.count == 0) return cudaSuccess;
+  groups.num_tiles = static_cast<int>(tiles);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (fp8) {
+    if (row || !col) return cudaErrorInvalidValue;  // MXFP8: column output only
+    return launch_had<false, true, true>(maps, groups, dev, stream);
+  }
+  if (row && col) return launch_had<true, true, false>(maps, groups, dev, stream);
+  if (row) return launch_had<true, false, false>(maps, groups, dev, stream);
+  return launch_had<false, true, false>(maps, groups, dev, stream);
+}
+
+cudaError_t launch_cast(const CastArgs& args, cudaStream_t stream) {
+  return launch_cast_grouped(&args, 1, stream);
 }
 
 }  // namespace mxfp4

@@ -24,6 +24,10 @@ struct CastArgs {
 
 // One launch over 128 x 128 tiles of x; writes whichever outputs are non-null.
 cudaError_t launch_cast(const CastArgs& args, cudaStream_t stream);
+// Up to 4 casts of one kind (the same outputs and element format; each its
+// own shape and Hadamard flags) in one launch, their tiles numbered one cast
+// after another; cudaErrorInvalidValue for count outside 1..4 or mixed kinds.
+cudaError_t launch_cast_grouped(const CastArgs* list, int count, cudaStream_t stream);
 
 // Makes the device that holds `data` current in this library's CUDA runtime
 // for the calling thread (binding its primary context); cudaErrorInvalidValue

@@ -132,6 +132,20 @@ def test_argument_validation_before_any_launch(L):
     assert grp(D(8, 8, 64, 8, a=odd)) == MIS                 # misaligned operand
     assert grp(D(8, 8, 64, 8, c=None)) == INV                # missing output
     assert grp(D(0, 8, 64, 8, c=None), D(8, 0, 64, 8, c=None)) == 0   # all empty: no-op
+    # grouped dual cast: the same rules, each descriptor checked as
+    # mxfp4_cast_dual checks its arguments
+    from quantization_mxfp4_cast_gb300 import CastDesc
+    C = lambda R, Cc, ldx, x=good, q=good, fl=0: CastDesc(x, R, Cc, ldx, q, good, good, good, fl)
+    cgrp = lambda *ds: L.mxfp4_cast_dual_grouped((CastDesc * len(ds))(*ds), len(ds), None)
+    assert L.mxfp4_cast_dual_grouped(None, 1, None) == INV
+    assert L.mxfp4_cast_dual_grouped((CastDesc * 1)(C(0, 64, 64)), 0, None) == INV
+    assert L.mxfp4_cast_dual_grouped((CastDesc * 5)(*[C(0, 64, 64)] * 5), 5, None) == INV
+    assert cgrp(C(48, 64, 64)) == INV                        # rows % 32
+    assert cgrp(C(0, 64, 64), C(32, 48, 64)) == INV          # second descriptor: cols % 32
+    assert cgrp(C(32, 64, 64, x=odd)) == MIS                 # misaligned input
+    assert cgrp(C(32, 64, 64, q=None)) == INV                # missing output
+    assert cgrp(C(32, 64, 64, fl=8)) == INV                  # unknown flag
+    assert cgrp(C(0, 64, 64, x=None), C(32, 0, 64, x=None)) == 0   # all empty: no-op
     st = ctypes.c_int(0)
     assert L.mxfp4_device_status(0, None) == INV
 

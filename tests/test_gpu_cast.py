@@ -195,3 +195,72 @@ def test_random_shapes_and_flags(m, seed):
                             frac=0.001)
     check_dual(m, x, had_row, had_col, linear)
     check_row(m, x, had_row, linear)
+
+
+def filled_dual_outputs(x, fill=0xAB):
+    # outputs pre-filled with a byte the cast never leaves behind, so every
+    # byte the two paths write (and every byte they leave alone) is compared
+    R, C = x.shape
+    import quantization_mxfp4_cast_gb300 as mod
+    u8 = lambda *s: torch.full(s, fill, dtype=torch.uint8, device=x.device)
+    return (u8(R, C // 2), u8(mod.scales_bytes(R, C)), u8(C, R // 2), u8(mod.scales_bytes(C, R)))
+
+
+def check_grouped_against_separate(m, items):
+    """items: (x, had_row, had_col) on the GPU.  The grouped call's bytes must
+    equal those of one mxfp4_cast_dual call per item."""
+    got = m.mxfp4_cast_dual_grouped([(x, hr, hc, filled_dual_outputs(x)) for x, hr, hc in items])
+    for (x, hr, hc), g in zip(items, got):
+        ref = m.mxfp4_cast_dual(x, hadamard_row=hr, hadamard_col=hc, out=filled_dual_outputs(x))
+        torch.cuda.synchronize()
+        for a, b, name in zip(g, ref, ("q_row", "sf_row", "q_col", "sf_col")):
+            assert torch.equal(a, b), f"{tuple(x.shape)} had_row={hr} had_col={hc}: {name} differs"
+    return got
+
+
+def test_grouped_dual_cast_step_shapes(m):
+    # the train step's three casts (X and dY with the column Hadamard, W
+    # without) in one launch, at a quarter of the token count
+    x = synth.normal_bf16((2048, 14336), 0.02, seed=1).cuda()
+    w = synth.normal_bf16((4096, 14336), 0.02, seed=2).cuda()
+    dy = synth.normal_bf16((2048, 4096), 1e-3, seed=3).cuda()
+    check_grouped_against_separate(m, [(x, False, True), (w, False, False), (dy, False, True)])
+
+
+def test_grouped_dual_cast_against_oracle(m):
+    # mixed shapes (ragged tiles, one slab, four casts) and every flag pair,
+    # checked byte for byte against the oracle
+    items = [(synth.with_outliers(synth.normal_bf16(s, 1.0, seed=70 + k), frac=0.01), hr, hc)
+             for k, (s, hr, hc) in enumerate([((96, 160), False, True), ((32, 32), True, True),
+                                              ((320, 224), False, False), ((256, 512), True, False)])]
+    got = m.mxfp4_cast_dual_grouped([(x.cuda(), hr, hc) for x, hr, hc in items])
+    torch.cuda.synchronize()
+    for (x, hr, hc), (qr, sr, qc, sc) in zip(items, got):
+        xb = bf16_bits(x)
+        cr, srr = oracle.cast_rows(xb, hadamard=hr)
+        cc, scc = oracle.cast_cols(xb, hadamard=hc)
+        assert np.array_equal(qr.cpu().numpy(), cr)
+        assert np.array_equal(qc.cpu().numpy(), cc)
+        assert np.array_equal(sr.cpu().numpy(), oracle.sf_linear_to_tile(srr))
+        assert np.array_equal(sc.cpu().numpy(), oracle.sf_linear_to_tile(scc))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_grouped_dual_cast_random(m, seed):
+    # 1-4 casts of random shapes (multiples of 32, up to a few dozen tiles)
+    # and random Hadamard flags, with an empty cast among them now and then
+    rng = np.random.default_rng(900 + seed)
+    n = int(rng.integers(1, 5))
+    items = []
+    for k in range(n):
+        R, C = 32 * int(rng.integers(1, 70)), 32 * int(rng.integers(1, 70))
+        if rng.random() < 0.15:
+            R = 0
+        x = synth.with_outliers(synth.normal_bf16((max(R, 32), C), float(rng.choice([1e-3, 1.0])),
+                                                  seed=950 + 10 * seed + k), frac=0.001)[:R].cuda()
+        items.append((x, bool(rng.integers(0, 2)), bool(rng.integers(0, 2))))
+    nonempty = [it for it in items if it[0].shape[0] > 0]
+    if nonempty:
+        check_grouped_against_separate(m, nonempty)
+    m.mxfp4_cast_dual_grouped([(x, hr, hc) for x, hr, hc in items])  # empty ones are skipped
+    torch.cuda.synchronize()
