@@ -19,13 +19,19 @@
 //     gridDim.x.  A producer thread streams their slabs with TMA (two 32 x 64
 //     boxes, 128-byte swizzle, zero fill past the edges) into a ring of 20
 //     slots (measured: 24 slots leave no room for the column-code buffers
-//     below, 16 are 4-8% slower); 15 consumer warps take the slabs in order from a shared counter
-//     as they become free, so the four slabs of a tile are quantized side by
+//     below, 16 are 4-8% slower); 15 consumer warps take the slabs in order
+//     from a shared counter as they become free, so the four slabs of a tile
+//     are quantized side by
 //     side (balanced to within one slab per SM, with loads in flight beyond the
 //     slabs being quantized).  A slot's sequence word tells a consumer when
 //     the producer has claimed the slot for its slab (and publishes the
 //     slab's coordinates), so no consumer waits on a barrier phase that
 //     belongs to an earlier use of the slot;
+//   * one launch may cast up to four tensors (mxfp4_cast_dual_grouped): their
+//     tiles are numbered one cast after another and every slab carries its
+//     cast's index, so the pipeline fills and drains once for all of them.
+//     Hadamard flags that differ between the casts are read per slab at run
+//     time; otherwise they are template parameters;
 //   * a tile's column codes (128 columns x 64 bytes: four 16-byte pieces per
 //     column, one from each slab's warp) and its two 512-byte scale tiles are
 //     assembled in shared memory; the warp that finishes the tile's last slab
