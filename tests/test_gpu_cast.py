@@ -264,3 +264,23 @@ def test_grouped_dual_cast_random(m, seed):
         check_grouped_against_separate(m, nonempty)
     m.mxfp4_cast_dual_grouped([(x, hr, hc) for x, hr, hc in items])  # empty ones are skipped
     torch.cuda.synchronize()
+
+
+def test_grouped_dual_cast_repeated_bit_identical(m):
+    # thirty back-to-back grouped launches of the step's three casts (full
+    # size: every SM runs many tiles, so the column-code staging buffers
+    # and the scale-tile buffers are reused many times over): every byte of
+    # every launch equal to the first launch's
+    x = synth.normal_bf16((8192, 14336), 0.02, seed=11).cuda()
+    w = synth.normal_bf16((4096, 14336), 0.02, seed=12).cuda()
+    dy = synth.normal_bf16((8192, 4096), 1e-3, seed=13).cuda()
+    items = [(x, False, True), (w, False, False), (dy, False, True)]
+    first = [tuple(t.clone() for t in o) for o in m.mxfp4_cast_dual_grouped(items)]
+    outs = [filled_dual_outputs(t) for t, _, _ in items]
+    for rep in range(30):
+        m.mxfp4_cast_dual_grouped([(t, hr, hc, o) for (t, hr, hc), o in zip(items, outs)])
+        torch.cuda.synchronize()
+        for k, (o, f) in enumerate(zip(outs, first)):
+            for a, b in zip(o, f):
+                assert torch.equal(a, b), f"launch {rep}, cast {k} differs"
+    assert m.device_status() == 0
