@@ -478,6 +478,31 @@ def cast_out_leg(step, stream, iters=20):
                     "Hadamard): separate cast kernel vs the cast written by the GEMM's epilogue"}
 
 
+def fwd_with_casts_leg(m, dev, stream, iters=10):
+    """The 8B gate/up forward from bf16 operands (X[8192, 4096] ~ N(0, 1),
+    W[28672, 4096] ~ N(0, 0.02)) through gemm_fp4_bf16_fwd: both row-wise
+    casts (one grouped launch), then the GEMM, against the GEMM alone on the
+    operands already cast.  CUDA events, back to back."""
+    M_, N_, K_, xs = synth.LLAMA_SHAPES["llama8b_gate_up"]
+    x = synth.normal_bf16((M_, K_), xs, seed=81).to(dev)
+    w = synth.normal_bf16((N_, K_), 0.02, seed=82).to(dev)
+    with torch.cuda.stream(stream):
+        y = torch.empty(M_, N_, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(m.workspace_bytes(m.MXFP4_OP_FWD, M_, N_, K_), dtype=torch.uint8, device=dev)
+        qx, qw = m.mxfp4_cast(x, stream=stream), m.mxfp4_cast(w, stream=stream)
+        full = lambda: m.gemm_fp4_bf16_fwd(x, w, y=y, ws=ws, stream=stream)
+        gemm = lambda: m.gemm_fp4(qx[0], qx[1], qw[0], qw[1], M_, N_, K_, c=y, stream=stream)
+        t_full = time_loop(full, iters, 3, stream)
+        t_gemm = time_loop(gemm, iters, 3, stream)
+    flop = 2.0 * M_ * N_ * K_
+    return {"unit": "TFLOP/s", "with_casts_tflops": flop / t_full / 1e12, "with_casts_us": t_full * 1e6,
+            "gemm_only_tflops": flop / t_gemm / 1e12, "gemm_only_us": t_gemm * 1e6,
+            "casts_us": (t_full - t_gemm) * 1e6,
+            "what": "Llama-3.1-8B gate/up forward Y[8192,28672] = X W^T from bf16 X and W: gemm_fp4_bf16_fwd "
+                    "(row-wise casts of X and W in one grouped launch, then the GEMM) against gemm_fp4 on the "
+                    "operands already cast (the weight cached)"}
+
+
 def time_each(fn, iters, stream, flush):
     """Mean seconds of fn() launched alone on `stream`, L2 overwritten before
     each launch (the flush sits outside the timed events)."""
@@ -1064,6 +1089,7 @@ def main():
         extra["dgrad_cast_out"] = cast_out_leg(step, stream)
         extra["cast_only"] = cast_only_leg(m, dev, stream, peaks["hbm"])
         extra["gemm_shapes"] = gemm_shapes_leg(m, dev, stream)
+        extra["gate_up_fwd_with_casts"] = fwd_with_casts_leg(m, dev, stream)
         extra["stack"] = stack_leg(dev, stream)
         if m.device_status() != 0:
             raise RuntimeError("device status word set in the layer leg")

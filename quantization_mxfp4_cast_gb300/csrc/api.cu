@@ -413,8 +413,8 @@ mxfp4_status gemm_fp8_bf16_wgrad(const uint16_t* dy, const uint16_t* x, uint16_t
   const uint32_t cf = ((flags & MXFP4_HADAMARD_COL) ? mxfp4::kFlagHadamardCol : 0u) | mxfp4::kFlagFp8;
   CastArgs cdy{dy, M, N, N, nullptr, nullptr, qdyt.q, qdyt.sf, cf};  // dY^T along M
   CastArgs cx{x, M, K, K, nullptr, nullptr, qxt.q, qxt.sf, cf};      // X^T along M
-  MXFP4_TRY(from_cuda(mxfp4::launch_cast(cdy, s)));
-  MXFP4_TRY(from_cuda(mxfp4::launch_cast(cx, s)));
+  const CastArgs casts[2] = {cdy, cx};  // one launch: the same kind of cast
+  MXFP4_TRY(from_cuda(mxfp4::launch_cast_grouped(casts, 2, s)));
   return gemm_checked(qdyt.q, qdyt.sf, qxt.q, qxt.sf, dw, N, K, M, K, s, true);
 }
 
@@ -442,8 +442,8 @@ mxfp4_status gemm_fp4_bf16_fwd(const uint16_t* x, const uint16_t* w, uint16_t* y
   QuantView qx = carve(cur, M, K), qw = carve(cur, N, K);
   CastArgs cx{x, M, K, K, qx.q, qx.sf, nullptr, nullptr, 0};
   CastArgs cw{w, N, K, K, qw.q, qw.sf, nullptr, nullptr, 0};
-  MXFP4_TRY(from_cuda(mxfp4::launch_cast(cx, s)));
-  MXFP4_TRY(from_cuda(mxfp4::launch_cast(cw, s)));
+  const CastArgs casts[2] = {cx, cw};  // one launch: both row-wise
+  MXFP4_TRY(from_cuda(mxfp4::launch_cast_grouped(casts, 2, s)));
   return gemm_checked(qx.q, qx.sf, qw.q, qw.sf, y, M, N, K, N, s);
 }
 
@@ -487,8 +487,8 @@ mxfp4_status gemm_fp4_bf16_wgrad(const uint16_t* dy, const uint16_t* x, uint16_t
   const uint32_t cf = (flags & MXFP4_HADAMARD_COL) ? mxfp4::kFlagHadamardCol : 0u;
   CastArgs cdy{dy, M, N, N, nullptr, nullptr, qdyt.q, qdyt.sf, cf};  // dY^T along M
   CastArgs cx{x, M, K, K, nullptr, nullptr, qxt.q, qxt.sf, cf};      // X^T along M
-  MXFP4_TRY(from_cuda(mxfp4::launch_cast(cdy, s)));
-  MXFP4_TRY(from_cuda(mxfp4::launch_cast(cx, s)));
+  const CastArgs casts[2] = {cdy, cx};  // one launch: the same kind of cast
+  MXFP4_TRY(from_cuda(mxfp4::launch_cast_grouped(casts, 2, s)));
   return gemm_checked(qdyt.q, qdyt.sf, qxt.q, qxt.sf, dw, N, K, M, K, s);
 }
 
